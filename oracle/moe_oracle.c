@@ -1,0 +1,374 @@
+/*
+ * moe_oracle.c -- plain CPU oracle for the MoE layer of a speculative
+ * verification pass.  TEST INFRASTRUCTURE ONLY: it is called by the tests,
+ * by __graft_entry__.smoke() and by the cpu_baseline leg of bench.py, and by
+ * nothing on the product path.  It shares no code, header, table or helper
+ * with the CUDA library; neither side includes or links the other.
+ *
+ * Everything is a plain per-token loop in double precision, written from the
+ * definitions on the pages, with no blocking, fusion or reordering:
+ *
+ *   router scores    s = W_g h, W_g in R^{N x d}
+ *                    ("Making Every Verified Token Count", Sec. 2.2, eq. (4))
+ *   top-k            indices of the k largest scores (same place); ties are
+ *                    broken toward the lower expert id and ids are emitted in
+ *                    descending score order (a reading: the pages are silent)
+ *   gate             softmax or sigmoid of the selected scores "depending on
+ *                    the architecture" (same place), three variants below
+ *   expert union     E_verify = union over verified tokens of S(x_t)
+ *                    ("Less Experts, Faster Decoding", eq. (1); "Making Every
+ *                    Verified Token Count", eq. (5); "The Limits of
+ *                    Speculation", App. A.4.1, eqs. (A1)-(A2))
+ *   expert FFN       SwiGLU: a = silu(W1 h) * (W3 h), o = W2 a, with the gate
+ *                    rows W1 stored before the up rows W3 (a reading)
+ *   layer output     y = sum_j w_j o_j  (+ the shared expert with weight 1)
+ *
+ * The deduplicating and per-slot engines of "Speculative Decoding for MoE
+ * Models: Expert Bytes, Kernel Bandwidth and the Best Draft Length"
+ * (abstract; Fig. 3) are two schedules of this same sum; the oracle computes
+ * the sum itself, once per (token, selected expert).
+ *
+ * Stored numbers are read from the very bytes the GPU receives:
+ *   bf16  -> double is exact (the 16 bits are the top half of an IEEE float);
+ *   e4m3  -> double is decoded from the OCP 8-bit floating point format
+ *            definition (1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ *            bits; exponent field 0 is subnormal; S.1111.111 is NaN; no
+ *            infinities), then multiplied by its fp32 128x128 block scale.
+ *
+ * Parity pins live in tests/test_oracle_pins.py; every function here has one.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* element types of stored arrays */
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+/* gate variants */
+enum { ORC_GATE_SOFTMAX = 0,        /* softmax over all experts, take the k  */
+       ORC_GATE_SOFTMAX_RENORM = 1, /* softmax restricted to the k selected  */
+       ORC_GATE_SIGMOID_RENORM = 2  /* sigmoid of the k, divided by its sum */
+};
+
+#define ORC_BLOCK 128 /* side of a square FP8 scale block */
+
+/* ---------------------------------------------------------------- decoding */
+
+double orc_bf16_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+double orc_f32_to_double(uint32_t bits) {
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* OCP FP8 E4M3: value = (-1)^s * 2^(e-7) * (1 + m/8) for e > 0,
+ *                       (-1)^s * 2^(-6)  * (m/8)     for e == 0,
+ * and NaN for e == 15, m == 7.  No infinities; largest finite is 448. */
+double orc_e4m3_to_double(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 3) & 15;
+  int m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* One stored element, as a double.  For E4M3 the caller applies the scale. */
+static double load_elem(const void *base, int type, size_t idx) {
+  switch (type) {
+  case ORC_F32: {
+    uint32_t b;
+    memcpy(&b, (const char *)base + 4 * idx, 4);
+    return orc_f32_to_double(b);
+  }
+  case ORC_BF16: {
+    uint16_t b;
+    memcpy(&b, (const char *)base + 2 * idx, 2);
+    return orc_bf16_to_double(b);
+  }
+  case ORC_E4M3:
+    return orc_e4m3_to_double(((const uint8_t *)base)[idx]);
+  }
+  return NAN;
+}
+
+/* ------------------------------------------------------------------ layer */
+
+typedef struct {
+  int d;          /* hidden size                                   */
+  int n_experts;  /* routed experts N                              */
+  int top_k;      /* experts per token k                           */
+  int inter;      /* SwiGLU intermediate size I                    */
+  int n_shared;   /* shared experts always applied (0 or 1)        */
+  int act_type;   /* ORC_F32 or ORC_BF16: h and W_g                */
+  int w_type;     /* ORC_F32, ORC_BF16 or ORC_E4M3: expert weights */
+  int gate;       /* ORC_GATE_*                                    */
+  const void *wg;  /* [N][d]                                        */
+  const void *w13; /* [N][2I][d]: rows 0..I-1 gate, rows I..2I-1 up */
+  const void *w2;  /* [N][d][I]                                     */
+  const float *s13; /* E4M3 only: [N][2I/128][d/128]                */
+  const float *s2;  /* E4M3 only: [N][d/128][I/128]                 */
+  const void *sh_w13; /* shared expert: [2I][d]                     */
+  const void *sh_w2;  /* shared expert: [d][I]                      */
+  const float *sh_s13;
+  const float *sh_s2;
+} orc_layer;
+
+/* Weight element (row, col) of a [rows][cols] matrix at `base`, with its
+ * block scale table `scale` ([rows/128][cols/128]) applied for E4M3. */
+static double weight_at(const orc_layer *L, const void *base,
+                        const float *scale, int rows, int cols, int row,
+                        int col) {
+  double v = load_elem(base, L->w_type, (size_t)row * cols + col);
+  (void)rows;
+  if (L->w_type == ORC_E4M3) {
+    int scale_cols = cols / ORC_BLOCK;
+    v *= (double)scale[(size_t)(row / ORC_BLOCK) * scale_cols + col / ORC_BLOCK];
+  }
+  return v;
+}
+
+static size_t elem_size(int type) {
+  return type == ORC_F32 ? 4 : type == ORC_BF16 ? 2 : 1;
+}
+
+/* Router scores of one token: z[e] = sum_i W_g[e][i] h[i]
+ * ("Making Every Verified Token Count", Sec. 2.2). */
+void orc_router_scores(const orc_layer *L, const double *h, double *z) {
+  for (int e = 0; e < L->n_experts; ++e) {
+    double acc = 0.0;
+    for (int i = 0; i < L->d; ++i)
+      acc += load_elem(L->wg, L->act_type, (size_t)e * L->d + i) * h[i];
+    z[e] = acc;
+  }
+}
+
+/* Order used by TopK: larger score first; equal scores, lower id first. */
+typedef struct {
+  double z;
+  int id;
+} scored;
+
+static int cmp_scored(const void *a, const void *b) {
+  const scored *x = (const scored *)a, *y = (const scored *)b;
+  if (x->z > y->z) return -1;
+  if (x->z < y->z) return 1;
+  return (x->id > y->id) - (x->id < y->id);
+}
+
+/* TopK of eq. (4): the k experts with the largest scores, by a full sort of
+ * all N scores. */
+void orc_topk(const double *z, int n_experts, int k, int32_t *ids) {
+  scored *s = (scored *)malloc(sizeof(scored) * (size_t)n_experts);
+  for (int e = 0; e < n_experts; ++e) {
+    s[e].z = z[e];
+    s[e].id = e;
+  }
+  qsort(s, (size_t)n_experts, sizeof(scored), cmp_scored);
+  for (int j = 0; j < k; ++j) ids[j] = s[j].id;
+  free(s);
+}
+
+/* Gate weights of the selected experts (eq. (4) and the sentence after it:
+ * "normalized ... by softmax or sigmoid depending on the architecture"). */
+void orc_gate(const double *z, int n_experts, const int32_t *ids, int k,
+              int gate, double *w) {
+  if (gate == ORC_GATE_SOFTMAX) {
+    double zmax = z[0];
+    for (int e = 1; e < n_experts; ++e)
+      if (z[e] > zmax) zmax = z[e];
+    double sum = 0.0;
+    for (int e = 0; e < n_experts; ++e) sum += exp(z[e] - zmax);
+    for (int j = 0; j < k; ++j) w[j] = exp(z[ids[j]] - zmax) / sum;
+  } else if (gate == ORC_GATE_SOFTMAX_RENORM) {
+    double zmax = z[ids[0]];
+    for (int j = 1; j < k; ++j)
+      if (z[ids[j]] > zmax) zmax = z[ids[j]];
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) sum += exp(z[ids[j]] - zmax);
+    for (int j = 0; j < k; ++j) w[j] = exp(z[ids[j]] - zmax) / sum;
+  } else {
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) {
+      w[j] = 1.0 / (1.0 + exp(-z[ids[j]]));
+      sum += w[j];
+    }
+    for (int j = 0; j < k; ++j) w[j] /= sum;
+  }
+}
+
+/* One expert's SwiGLU FFN on one token, accumulated into y with weight wt:
+ *   g_i = W1[i] . h,  u_i = W3[i] . h,  a_i = g_i * sigmoid(g_i) * u_i,
+ *   o_r = W2[r] . a,  y_r += wt * o_r. */
+static void expert_ffn(const orc_layer *L, const void *w13, const float *s13,
+                       const void *w2, const float *s2, const double *h,
+                       double wt, double *a, double *y) {
+  int d = L->d, I = L->inter;
+  for (int i = 0; i < I; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int c = 0; c < d; ++c) {
+      g += weight_at(L, w13, s13, 2 * I, d, i, c) * h[c];
+      u += weight_at(L, w13, s13, 2 * I, d, I + i, c) * h[c];
+    }
+    a[i] = g / (1.0 + exp(-g)) * u;
+  }
+  for (int r = 0; r < d; ++r) {
+    double o = 0.0;
+    for (int i = 0; i < I; ++i) o += weight_at(L, w2, s2, d, I, r, i) * a[i];
+    y[r] += wt * o;
+  }
+}
+
+/* Pointers to expert e's matrices inside the expert-major arrays. */
+static void expert_ptrs(const orc_layer *L, int e, const void **w13,
+                        const float **s13, const void **w2, const float **s2) {
+  size_t es = elem_size(L->w_type);
+  size_t n13 = (size_t)2 * L->inter * L->d, n2 = (size_t)L->d * L->inter;
+  *w13 = (const char *)L->w13 + (size_t)e * n13 * es;
+  *w2 = (const char *)L->w2 + (size_t)e * n2 * es;
+  *s13 = NULL;
+  *s2 = NULL;
+  if (L->w_type == ORC_E4M3) {
+    *s13 = L->s13 + (size_t)e * (n13 / (ORC_BLOCK * ORC_BLOCK));
+    *s2 = L->s2 + (size_t)e * (n2 / (ORC_BLOCK * ORC_BLOCK));
+  }
+}
+
+/* The whole layer for one token t. */
+static void verify_token(const orc_layer *L, const void *hs, int t,
+                         int32_t *ids, double *w, double *z, double *y) {
+  int d = L->d;
+  double *h = (double *)malloc(sizeof(double) * (size_t)d);
+  double *a = (double *)malloc(sizeof(double) * (size_t)L->inter);
+  for (int c = 0; c < d; ++c)
+    h[c] = load_elem(hs, L->act_type, (size_t)t * d + c);
+  orc_router_scores(L, h, z);
+  orc_topk(z, L->n_experts, L->top_k, ids);
+  orc_gate(z, L->n_experts, ids, L->top_k, L->gate, w);
+  for (int r = 0; r < d; ++r) y[r] = 0.0;
+  for (int j = 0; j < L->top_k; ++j) {
+    const void *w13, *w2;
+    const float *s13, *s2;
+    expert_ptrs(L, ids[j], &w13, &s13, &w2, &s2);
+    expert_ffn(L, w13, s13, w2, s2, h, w[j], a, y);
+  }
+  for (int s = 0; s < L->n_shared; ++s)
+    expert_ffn(L, L->sh_w13, L->sh_s13, L->sh_w2, L->sh_s2, h, 1.0, a, y);
+  free(a);
+  free(h);
+}
+
+typedef struct {
+  const orc_layer *L;
+  const void *hs;
+  const int32_t *tokens;
+  int n_tokens;
+  int stride;
+  int first;
+  int32_t *ids;
+  double *w, *z, *y;
+} worker_arg;
+
+static void *worker(void *p) {
+  worker_arg *A = (worker_arg *)p;
+  for (int i = A->first; i < A->n_tokens; i += A->stride) {
+    int t = A->tokens ? A->tokens[i] : i;
+    verify_token(A->L, A->hs, t, A->ids + (size_t)i * A->L->top_k,
+                 A->w + (size_t)i * A->L->top_k,
+                 A->z + (size_t)i * A->L->n_experts, A->y + (size_t)i * A->L->d);
+  }
+  return NULL;
+}
+
+/* The verification pass for the tokens listed in `tokens` (all n tokens in
+ * order when `tokens` is NULL; then n_tokens = n).  Output row i belongs to
+ * token tokens[i].  Tokens are independent, so the loop may be split across
+ * n_threads host threads without changing any result. */
+int orc_verify(const orc_layer *L, const void *hs, const int32_t *tokens,
+               int n_tokens, int n_threads, int32_t *ids, double *w, double *z,
+               double *y) {
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > n_tokens) n_threads = n_tokens > 0 ? n_tokens : 1;
+  if (n_threads == 1) {
+    worker_arg A = {L, hs, tokens, n_tokens, 1, 0, ids, w, z, y};
+    worker(&A);
+    return 0;
+  }
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+  worker_arg *A = (worker_arg *)malloc(sizeof(worker_arg) * (size_t)n_threads);
+  for (int i = 0; i < n_threads; ++i) {
+    worker_arg a = {L, hs, tokens, n_tokens, n_threads, i, ids, w, z, y};
+    A[i] = a;
+    pthread_create(&th[i], NULL, worker, &A[i]);
+  }
+  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  free(A);
+  free(th);
+  return 0;
+}
+
+/* TopK and gate on given fp32 scores (the same ordering, on exactly the
+ * numbers a GPU produced, widened to double without rounding). */
+void orc_topk_from_scores(const float *scores, int n, int n_experts, int k,
+                          int gate, int32_t *ids, double *w) {
+  double *z = (double *)malloc(sizeof(double) * (size_t)n_experts);
+  for (int t = 0; t < n; ++t) {
+    for (int e = 0; e < n_experts; ++e)
+      z[e] = (double)scores[(size_t)t * n_experts + e];
+    orc_topk(z, n_experts, k, ids + (size_t)t * k);
+    orc_gate(z, n_experts, ids + (size_t)t * k, k, gate, w + (size_t)t * k);
+  }
+  free(z);
+}
+
+/* ------------------------------------------------------------ union plan */
+
+/* The union of the routed experts of all n tokens and the grouping of the
+ * n*k (token, slot) pairs by expert ("Less Experts, Faster Decoding", eq. (1);
+ * "Making Every Verified Token Count", eq. (5)).
+ *   hist[e]   number of slots that name expert e
+ *   uniq[u]   the distinct experts, ascending (u < U)
+ *   offs[u]   first position of expert uniq[u]'s group in perm; offs[U] = n*k
+ *   perm[p]   slot indices t*k+j, grouped by expert in uniq order, ascending
+ *             slot index inside a group
+ * Returns U. */
+int orc_union_plan(const int32_t *ids, int n_slots, int n_experts,
+                   int32_t *hist, int32_t *uniq, int32_t *offs,
+                   int32_t *perm) {
+  int U = 0;
+  for (int e = 0; e < n_experts; ++e) hist[e] = 0;
+  for (int p = 0; p < n_slots; ++p) hist[ids[p]] += 1;
+  for (int e = 0; e < n_experts; ++e)
+    if (hist[e] > 0) uniq[U++] = e;
+  int pos = 0;
+  for (int u = 0; u < U; ++u) {
+    offs[u] = pos;
+    for (int p = 0; p < n_slots; ++p)
+      if (ids[p] == uniq[u]) perm[pos++] = p;
+  }
+  offs[U] = pos;
+  return U;
+}
+
+/* Bytes of one expert: the three d x I matrices, plus, for E4M3, the fp32
+ * block scales ("Less Experts, Faster Decoding", Fig. 1(c): one FP8 expert of
+ * a 7168 x 2048 layer is 44.04 MB). */
+void orc_expert_bytes(int d, int inter, int w_type, int64_t *weights,
+                      int64_t *scales) {
+  *weights = (int64_t)3 * d * inter * (int64_t)elem_size(w_type);
+  *scales = 0;
+  if (w_type == ORC_E4M3)
+    *scales = (int64_t)4 * (((int64_t)2 * inter / ORC_BLOCK) * (d / ORC_BLOCK) +
+                            ((int64_t)d / ORC_BLOCK) * (inter / ORC_BLOCK));
+}

@@ -1,0 +1,52 @@
+"""The pins must fail on a broken oracle.
+
+Each case plants one plausible mistake in a copy of the oracle's C source,
+builds it into a temporary library, and runs the pin suite against it in a
+child process: the suite has to fail.  Everything runs on the CPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "gate_and_up_swapped": ("g += weight_at(L, w13, s13, 2 * I, d, i, c) * h[c];",
+                            "g += weight_at(L, w13, s13, 2 * I, d, I + i, c) * h[c];"),
+    "down_projection_transposed": ("o += weight_at(L, w2, s2, d, I, r, i) * a[i];",
+                                   "o += weight_at(L, w2, s2, I, d, i, r) * a[i];"),
+    "scale_block_transposed": ("scale[(size_t)(row / ORC_BLOCK) * scale_cols + col / ORC_BLOCK]",
+                               "scale[(size_t)(col / ORC_BLOCK) * scale_cols + row / ORC_BLOCK]"),
+    "ties_to_higher_id": ("return (x->id > y->id) - (x->id < y->id);",
+                          "return (x->id < y->id) - (x->id > y->id);"),
+    "e4m3_bias_8": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+                    "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "subnormal_exponent": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    "shared_expert_dropped": ("for (int s = 0; s < L->n_shared; ++s)", "for (int s = 0; s < 0; ++s)"),
+    "silu_without_gate_factor": ("a[i] = g / (1.0 + exp(-g)) * u;", "a[i] = 1.0 / (1.0 + exp(-g)) * u;"),
+    "softmax_not_renormalised": ("for (int j = 0; j < k; ++j) w[j] = exp(z[ids[j]] - zmax) / sum;\n  } else {",
+                                 "for (int j = 0; j < k; ++j) w[j] = exp(z[ids[j]] - zmax);\n  } else {"),
+    "plan_not_stable": ("for (int p = 0; p < n_slots; ++p)\n      if (ids[p] == uniq[u]) perm[pos++] = p;",
+                        "for (int p = n_slots - 1; p >= 0; --p)\n      if (ids[p] == uniq[u]) perm[pos++] = p;"),
+    "scale_bytes_dropped": ("*scales = (int64_t)4 *", "*scales = (int64_t)0 *"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mut = tmp_path / "mut.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           "-o", str(lib), str(mut), "-lm"])
+    env = dict(os.environ, MOE_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins passed on mutant {name}:\n{r.stdout[-2000:]}"

@@ -1,0 +1,359 @@
+"""Pins of the CPU oracle against facts fixed by the pages or by mathematics.
+
+Nothing here compares the oracle with itself: each check uses a closed form,
+a brute-force enumeration, an independent library routine (torch's float8 /
+bfloat16 casts, scipy's softmax and expit, numpy's matmul), an invariant, or
+a number the pages print.  Each is chosen so that a plausible slip in the
+oracle (a swapped gate/up, a transposed down projection, a wrong scale block
+index, a tie broken the other way, a dropped shared expert) fails it.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle as O
+
+
+# ----------------------------------------------------------------- decoding
+
+def test_e4m3_decode_all_256_codes_against_torch_cast():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = O.decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # zero's sign survives
+    assert math.copysign(1.0, ours[0x80]) == -1.0
+
+
+def test_e4m3_decode_format_facts():
+    # OCP E4M3: bias 7, largest finite 448, smallest subnormal 2^-9,
+    # smallest normal 2^-6, only S.1111.111 is NaN, no infinities.
+    d = O.decode_e4m3(np.arange(256, dtype=np.uint8))
+    assert d[0x38] == 1.0
+    assert d[0x7E] == 448.0 and d[0xFE] == -448.0
+    assert d[0x01] == 2.0 ** -9 and d[0x07] == 7 * 2.0 ** -9
+    assert d[0x08] == 2.0 ** -6
+    assert np.isnan(d[0x7F]) and np.isnan(d[0xFF])
+    assert np.sum(np.isnan(d)) == 2 and not np.any(np.isinf(d))
+    finite = d[~np.isnan(d)]
+    assert np.max(finite) == 448.0
+
+
+def test_bf16_decode_against_torch():
+    g = torch.Generator().manual_seed(11)
+    x = (torch.randn(4096, generator=g) * 10).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.bf16_to_double(bits), x.to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------------- top-k
+
+def _brute_topk(z, k):
+    """The unique k-subset S whose members all beat every non-member under
+    (larger score, then lower id), listed in that order."""
+    E = len(z)
+    beats = lambda i, j: z[i] > z[j] or (z[i] == z[j] and i < j)
+    found = [S for S in itertools.combinations(range(E), k)
+             if all(beats(i, j) for i in S for j in range(E) if j not in S)]
+    assert len(found) == 1
+    return sorted(found[0], key=lambda i: (-z[i], i))
+
+
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("k", [1, 2, 4])
+def test_topk_brute_force_on_16_experts(ties, k):
+    rng = np.random.default_rng(100 + k + 10 * ties)
+    for _ in range(40):
+        z = (rng.integers(-3, 4, size=16).astype(np.float64) if ties
+             else rng.standard_normal(16))
+        assert list(O.topk(z, k)) == _brute_topk(list(z), k)
+
+
+def test_topk_matches_numpy_lexsort():
+    rng = np.random.default_rng(3)
+    for E, k in [(64, 8), (128, 8), (128, 4), (256, 8)]:
+        z = np.round(rng.standard_normal(E), 1)     # many ties
+        expect = np.lexsort((np.arange(E), -z))[:k]
+        assert np.array_equal(O.topk(z, k), expect)
+
+
+def test_topk_from_scores_signed_zero_is_a_tie():
+    s = np.array([[0.0, -0.0, -1.0, 0.0]], dtype=np.float32)
+    ids, _ = O.topk_from_scores(s, 3, O.GATE_SOFTMAX_RENORM)
+    assert list(ids[0]) == [0, 1, 3]
+
+
+# -------------------------------------------------------------------- gates
+
+def test_gates_against_scipy():
+    rng = np.random.default_rng(4)
+    for E, k in [(16, 2), (64, 8), (256, 8)]:
+        z = rng.standard_normal(E) * 3
+        ids = O.topk(z, k)
+        p = scipy.special.softmax(z)
+        w = O.gate(z, ids, O.GATE_SOFTMAX)
+        np.testing.assert_allclose(w, p[ids], rtol=1e-13)
+        assert w.sum() < 1.0
+        w = O.gate(z, ids, O.GATE_SOFTMAX_RENORM)
+        np.testing.assert_allclose(w, scipy.special.softmax(z[ids]), rtol=1e-13)
+        np.testing.assert_allclose(w, p[ids] / p[ids].sum(), rtol=1e-12)
+        assert abs(w.sum() - 1.0) < 1e-14
+        w = O.gate(z, ids, O.GATE_SIGMOID_RENORM)
+        sg = scipy.special.expit(z[ids])
+        np.testing.assert_allclose(w, sg / sg.sum(), rtol=1e-13)
+
+
+# ----------------------------------------------------------------- the FFN
+
+def _f32_layer(d, I, E, k, gate, wg, w13, w2, sh=None):
+    f = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+    return O.Layer(d, E, k, I, O.F32, O.F32, gate, f(wg), f(w13), f(w2),
+                   sh_w13=f(sh[0]) if sh else None, sh_w2=f(sh[1]) if sh else None)
+
+
+def test_swiglu_closed_form_gate_rows_first_and_down_layout():
+    # one expert, h = e_0: gate pre-activations g_i = W1[i][0], up = W3[i][0] = 1,
+    # so a_i = silu(g_i); W2 = [[1,0,0],[0,1,0],[0,0,1],[1,1,1]] reads a back.
+    d, I = 4, 3
+    g = [1.0, -2.0, 0.5]
+    w13 = np.zeros((1, 2 * I, d))
+    for i in range(I):
+        w13[0, i, 0] = g[i]       # gate rows first
+        w13[0, I + i, 0] = 1.0    # then up rows
+    w2 = np.zeros((1, d, I))
+    w2[0, :I, :] = np.eye(I)
+    w2[0, I, :] = 1.0
+    wg = np.ones((1, d))
+    L = _f32_layer(d, I, 1, 1, O.GATE_SOFTMAX_RENORM, wg, w13, w2)
+    h = np.array([[1.0, 0.0, 0.0, 0.0]], dtype=np.float32)
+    ids, w, z, y = O.verify(L, h)
+    silu = [0.7310585786300049, -0.2384058440442351, 0.31122966560092724]  # x / (1 + e^-x)
+    np.testing.assert_allclose(y[0], silu + [sum(silu)], rtol=1e-15, atol=1e-16)
+    assert w[0, 0] == 1.0 and z[0, 0] == 1.0
+
+
+def test_router_scores_and_selection_closed_form():
+    # W_g = identity on 4 experts: scores equal h; experts 2 and 0 win.
+    d = I = 4
+    E, k = 4, 2
+    wg = np.eye(E, d)
+    w13 = np.zeros((E, 2 * I, d))
+    w2 = np.zeros((E, d, I))
+    for e in range(E):          # expert e: a_0 = silu(1)*1 at h[0]=1 -> y = (e+1) e_0
+        w13[e, 0, 0] = 1.0
+        w13[e, I, 0] = 1.0
+        w2[e, 0, 0] = e + 1.0
+    h = np.array([[1.0, -0.5, 3.0, 0.25]], dtype=np.float32)
+    L = _f32_layer(d, I, E, k, O.GATE_SOFTMAX_RENORM, wg, w13, w2)
+    ids, w, z, y = O.verify(L, h)
+    np.testing.assert_array_equal(z[0], h[0])
+    assert list(ids[0]) == [2, 0]
+    e3, e1 = math.exp(3.0), math.exp(1.0)
+    silu1 = 1.0 / (1.0 + math.exp(-1.0))
+    expect = (e3 * 3.0 + e1 * 1.0) / (e3 + e1) * silu1
+    assert abs(y[0, 0] - expect) < 1e-14 and np.all(y[0, 1:] == 0)
+
+
+def _dense_numpy(wg, w13, w2, h, k, gate, sh=None):
+    """Every expert applied to every token with numpy matmuls, then the top-k
+    picked by numpy's lexsort and gated with scipy."""
+    I = w13.shape[1] // 2
+    z = h @ wg.T
+    out = np.zeros((h.shape[0], w2.shape[1]))
+    for t in range(h.shape[0]):
+        ids = np.lexsort((np.arange(z.shape[1]), -z[t]))[:k]
+        if gate == O.GATE_SOFTMAX:
+            wts = scipy.special.softmax(z[t])[ids]
+        elif gate == O.GATE_SOFTMAX_RENORM:
+            wts = scipy.special.softmax(z[t, ids])
+        else:
+            s = scipy.special.expit(z[t, ids])
+            wts = s / s.sum()
+        allo = []
+        for e in range(wg.shape[0]):
+            gu = w13[e] @ h[t]
+            a = gu[:I] * scipy.special.expit(gu[:I]) * gu[I:]
+            allo.append(w2[e] @ a)
+        out[t] = sum(wts[j] * allo[ids[j]] for j in range(k))
+        if sh is not None:
+            gu = sh[0] @ h[t]
+            out[t] += sh[1] @ (gu[:I] * scipy.special.expit(gu[:I]) * gu[I:])
+    return out
+
+
+@pytest.mark.parametrize("gate", [O.GATE_SOFTMAX, O.GATE_SOFTMAX_RENORM, O.GATE_SIGMOID_RENORM])
+@pytest.mark.parametrize("shared", [False, True])
+def test_layer_against_dense_numpy_formulation(gate, shared):
+    rng = np.random.default_rng(9 + gate + 3 * shared)
+    d, I, E, k, n = 24, 10, 6, 2, 5           # d != I catches a transposed W2
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    wg, w13, w2, h = f(E, d), f(E, 2 * I, d) * 0.3, f(E, d, I) * 0.3, f(n, d)
+    sh = (f(2 * I, d) * 0.3, f(d, I) * 0.3) if shared else None
+    L = _f32_layer(d, I, E, k, gate, wg, w13, w2, sh)
+    _, _, _, y = O.verify(L, h)
+    ref = _dense_numpy(wg.astype(np.float64), w13.astype(np.float64), w2.astype(np.float64),
+                       h.astype(np.float64), k, gate,
+                       None if sh is None else tuple(s.astype(np.float64) for s in sh))
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_layer_is_linear_in_down_weights_and_invariant_to_expert_relabeling():
+    rng = np.random.default_rng(21)
+    d, I, E, k, n = 16, 8, 8, 3, 4
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    wg, w13, w2, h = f(E, d), f(E, 2 * I, d), f(E, d, I), f(n, d)
+    _, _, _, y = O.verify(_f32_layer(d, I, E, k, O.GATE_SIGMOID_RENORM, wg, w13, w2), h)
+    _, _, _, y4 = O.verify(_f32_layer(d, I, E, k, O.GATE_SIGMOID_RENORM, wg, w13, 4 * w2), h)
+    np.testing.assert_allclose(y4, 4 * y, rtol=1e-12)
+    p = rng.permutation(E)
+    ids0, _, _, _ = O.verify(_f32_layer(d, I, E, k, O.GATE_SIGMOID_RENORM, wg, w13, w2), h)
+    idsp, _, _, yp = O.verify(_f32_layer(d, I, E, k, O.GATE_SIGMOID_RENORM,
+                                         wg[p], w13[p], w2[p]), h)
+    np.testing.assert_allclose(yp, y, rtol=1e-12, atol=1e-14)
+    # new expert i is old expert p[i]
+    assert sorted(p[idsp].ravel().tolist()) == sorted(ids0.ravel().tolist())
+
+
+def test_bf16_layer_reads_the_stored_bits():
+    # a bf16 layer equals the f32 layer built from the same (exact) values
+    rng = np.random.default_rng(31)
+    d, I, E, k, n = 16, 8, 4, 2, 3
+    tb = lambda *s: torch.from_numpy(rng.standard_normal(s).astype(np.float32)).to(torch.bfloat16)
+    wg, w13, w2, h = tb(E, d), tb(E, 2 * I, d), tb(E, d, I), tb(n, d)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    Lb = O.Layer(d, E, k, I, O.BF16, O.BF16, O.GATE_SOFTMAX, bits(wg), bits(w13), bits(w2))
+    _, _, _, yb = O.verify(Lb, bits(h))
+    f = lambda t: t.to(torch.float32).numpy()
+    _, _, _, yf = O.verify(_f32_layer(d, I, E, k, O.GATE_SOFTMAX, f(wg), f(w13), f(w2)), f(h))
+    np.testing.assert_array_equal(yb, yf)
+
+
+def test_e4m3_block_scale_indexing_one_hot():
+    # One nonzero code per matrix, placed in a chosen 128x128 block whose scale
+    # differs from every other block: the output isolates scale[row/128][col/128]
+    # of both W13 (gate and up) and W2.
+    d, I, E = 256, 256, 1
+    w13 = np.zeros((1, 2 * I, d), np.uint8)
+    w2 = np.zeros((1, d, I), np.uint8)
+    s13 = (np.arange(4 * 2, dtype=np.float32).reshape(1, 4, 2) + 1.0) * 0.5  # [2I/128][d/128]
+    s2 = (np.arange(2 * 2, dtype=np.float32).reshape(1, 2, 2) + 1.0) * 0.25  # [d/128][I/128]
+    i, c, r = 131, 200, 7                    # gate row i (block 1), column c (block 1)
+    w13[0, i, c] = 0x38                      # 1.0
+    w13[0, I + i, c] = 0x40                  # 2.0 (up row I+i sits in row block 3)
+    w2[0, r, i] = 0x30                       # 0.5, row block 0, column block 1
+    L = O.Layer(d, E, 1, I, O.F32, O.E4M3, O.GATE_SOFTMAX_RENORM,
+                np.zeros((1, d), np.float32), w13, w2, s13, s2)
+    h = np.zeros((1, d), np.float32)
+    h[0, c] = 0.75
+    _, _, _, y = O.verify(L, h)
+    g = 1.0 * float(s13[0, 1, 1]) * 0.75
+    u = 2.0 * float(s13[0, 3, 1]) * 0.75
+    a = g / (1 + math.exp(-g)) * u
+    expect = np.zeros(d)
+    expect[r] = 0.5 * float(s2[0, 0, 1]) * a
+    np.testing.assert_allclose(y[0], expect, rtol=1e-15, atol=0)
+
+
+def test_shared_expert_adds_with_weight_one():
+    rng = np.random.default_rng(41)
+    d, I, E, k, n = 8, 4, 4, 2, 3
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    wg, w13, w2, h = f(E, d), f(E, 2 * I, d), f(E, d, I), f(n, d)
+    sh13, sh2 = f(2 * I, d), f(d, I)
+    _, _, _, y0 = O.verify(_f32_layer(d, I, E, k, O.GATE_SIGMOID_RENORM, wg, w13, w2), h)
+    # the shared expert alone: a one-expert layer with k = 1 and weight 1
+    _, _, _, ys = O.verify(_f32_layer(d, I, 1, 1, O.GATE_SOFTMAX_RENORM, wg[:1],
+                                      sh13[None], sh2[None]), h)
+    _, _, _, y1 = O.verify(_f32_layer(d, I, E, k, O.GATE_SIGMOID_RENORM, wg, w13, w2,
+                                      (sh13, sh2)), h)
+    np.testing.assert_allclose(y1, y0 + ys, rtol=1e-12, atol=1e-14)
+
+
+def test_token_subset_and_threads_do_not_change_results():
+    rng = np.random.default_rng(51)
+    d, I, E, k, n = 16, 8, 8, 2, 7
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    L = _f32_layer(d, I, E, k, O.GATE_SOFTMAX, f(E, d), f(E, 2 * I, d), f(E, d, I))
+    h = f(n, d)
+    ids, w, z, y = O.verify(L, h)
+    ids3, w3, z3, y3 = O.verify(L, h, threads=3)
+    assert np.array_equal(y, y3) and np.array_equal(ids, ids3)
+    sel = [6, 2, 2]
+    idss, _, _, ys = O.verify(L, h, tokens=sel, threads=2)
+    assert np.array_equal(ys, y[sel]) and np.array_equal(idss, ids[sel])
+
+
+# -------------------------------------------------------------- union plan
+
+def _check_plan(ids, E, k):
+    U, hist, uniq, offs, perm = O.union_plan(ids, E)
+    flat = np.asarray(ids).ravel()
+    n = flat.size // k
+    assert U == len(set(flat.tolist()))
+    assert hist.sum() == flat.size
+    assert np.all(np.diff(uniq) > 0)
+    assert sorted(perm.tolist()) == list(range(flat.size))
+    for u in range(U):
+        seg = perm[offs[u]:offs[u + 1]]
+        assert np.all(flat[seg] == uniq[u]) and np.all(np.diff(seg) > 0)
+        assert offs[u + 1] - offs[u] == hist[uniq[u]]
+    assert k <= U <= min(E, n * k)
+    # "Expert Bytes ...", Fig. 3: U/(nm) lies between 1/n and 1
+    assert 1.0 / n - 1e-15 <= U / (n * k) <= 1.0
+    return U
+
+
+def test_union_plan_invariants_random_ids():
+    for (n, k, E, seed) in [(1, 2, 16, 1), (4, 2, 16, 2), (8, 8, 64, 3), (16, 8, 128, 4),
+                            (64, 8, 256, 5), (13, 4, 128, 6)]:
+        ids = torch.stack([torch.randperm(E, generator=torch.Generator().manual_seed(seed * 100 + t))[:k]
+                           for t in range(n)]).numpy()
+        _check_plan(ids, E, k)
+
+
+def test_identical_tokens_give_a_union_of_exactly_k():
+    row = np.array([5, 17, 3, 250, 9, 0, 128, 77], dtype=np.int32)
+    for n in (1, 2, 8, 64):
+        ids = np.tile(row, (n, 1))
+        assert _check_plan(ids, 256, 8) == 8
+
+
+def test_disjoint_tokens_give_a_union_of_nk():
+    ids = np.arange(64, dtype=np.int32).reshape(8, 8)
+    assert _check_plan(ids, 64, 8) == 64
+
+
+def test_uniform_routing_mean_union_matches_closed_form():
+    # independent uniform k-subsets: P(e unused by all n tokens) = (1-k/E)^n,
+    # so E[U] = E (1 - (1 - k/E)^n)   ("Expert Bytes ...", Fig. 1: 1 - q^(n-1))
+    from moe_expert_ffn_gemv_gb300 import synth
+    for n, k, E in [(2, 8, 64), (8, 8, 256), (16, 4, 128), (64, 8, 256)]:
+        Us = []
+        for rep in range(300):
+            ids = synth.uniform_ids(n, k, E, seed=1000 * n + rep).numpy()
+            Us.append(O.union_plan(ids, E)[0])
+        Us = np.array(Us, dtype=np.float64)
+        expect = E * (1 - (1 - k / E) ** n)
+        se = Us.std(ddof=1) / math.sqrt(len(Us))
+        assert abs(Us.mean() - expect) < 3.5 * se + 1e-9, (n, k, E, Us.mean(), expect, se)
+
+
+# -------------------------------------------------------------- byte counts
+
+def test_expert_bytes_printed_on_the_pages():
+    # "Less Experts, Faster Decoding", Fig. 1(c): one DeepSeek-V3.1 FP8 expert
+    # moves 44.04 MB; 3 * 7168 * 2048 * 1 B = 44,040,192 B.
+    wb, sb = O.expert_bytes(7168, 2048, O.E4M3)
+    assert wb == 44_040_192 and round(wb / 1e6, 2) == 44.04
+    assert sb == 4 * (32 * 56 + 56 * 16) == 10_752
+    # "The Limits of Speculation", App. A.6: 9.4 MB per Qwen3-30B-A3B bf16 expert
+    wb, sb = O.expert_bytes(2048, 768, O.BF16)
+    assert wb == 9_437_184 and round(wb / 1e6, 1) == 9.4 and sb == 0
+    # and 48 layers of it is about 0.45 GB
+    assert round(48 * wb / 1e9, 2) == 0.45
