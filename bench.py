@@ -1,0 +1,459 @@
+"""Benchmark of the MoE verification pass on GB300.
+
+Workload: the DeepSeek-V3-shaped FP8-E4M3 layer (d 7168, 256 routed experts
+top-8 with sigmoid gating, 1 shared expert, intermediate 2048, 128x128 fp32
+block scales), n = 8 draft-tree tokens (BFS tree, 4 children under the root,
+2 below; child = 0.6 parent + 0.8 eps).  Synthetic, seeded weights and
+hidden states; weights resident in HBM.
+
+One step = one verification pass through the C ABI: router scores + top-k
+(moe_route_topk), union plan (moe_union_plan), the deduplicating expert FFN
+and combine (moe_verify_dedup).  `value` = union-expert bytes per pass
+(routed union + shared expert, weights and scales) / device time per pass.
+The expert bytes of one pass (~2.5 GB) exceed the 129 MB L2, so passes run
+back to back with no flush.
+
+Also printed: the expert kernels' roofline against the measured HBM copy
+bandwidth, the end-to-end number (hidden states copied from pinned host
+memory, outputs copied back, every step), the oracle on the host cores, and
+a dedup-vs-per-slot sweep over n = 1..64 with its crossover.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_ffn_gemv_gb300 import synth  # noqa: E402
+
+CFG = synth.DSV3
+N_TOKENS = 8
+METRIC = "µs per MoE verify pass and union-byte HBM GB/s (% of GB300 peak) vs n tokens"
+WORKLOAD = "deepseek-v3-shaped fp8-e4m3 moe layer, n=8 draft-tree tokens (rho=0.6), dedup verify pass"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_PASS = 7  # router scores, top-k, plan, bf16->fp16, gate/up, down, combine
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-sweep", action="store_true", help="skip the n = 1..64 engine sweep")
+    p.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    p.add_argument("--sweep-max", type=int, default=64)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------- environment
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_from_profile():
+    """DRAM bytes per dedup call from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dedup_dsv3_fp8_n8.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic_json:"):
+                    j = json.loads(line.split(":", 1)[1])
+                    if j.get("csrc_sha256") == csrc_hash():
+                        return j.get("dram_bytes_per_dedup_call")
+    except Exception:
+        pass
+    return None
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "moe_expert_ffn_gemv_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# -------------------------------------------------------------- workloads
+
+def make_workload(device="cuda"):
+    layer = synth.make_layer(CFG, seed=1, device=device)
+    h = synth.make_hidden(CFG, 64, seed=3, device=device)   # the first n nodes of a 64-node tree
+    return layer, h
+
+
+def expert_bytes(mv, desc):
+    wb, sb = mv.moe_expert_bytes(desc)
+    return wb + sb
+
+
+# ------------------------------------------------------------------- ours
+
+def run_ours(args):
+    ws, rank = dist_setup(args)
+    from moe_expert_ffn_gemv_gb300 import binding as mv
+    n = N_TOKENS
+    layer, h_all = make_workload()
+    h = h_all[:n].contiguous()
+    vl = mv.VerifyLayer(layer, 64)
+    eb = expert_bytes(mv, vl.desc)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 3)):
+        vl.verify_pass(h, n)
+    assert vl.last_error() == 0
+    union_bytes = int(vl.plan.union_bytes[0])
+    U = int(vl.plan.n_uniq[0])
+
+    # timed region: K passes back to back; events around the pass and around
+    # the expert call (the dominant kernels) on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            vl.route(h, n)
+            vl.union_plan(n)
+            ev[i][1].record(stream)
+            vl.dedup(h, n)
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws)
+    assert vl.last_error() == 0
+    pass_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    dedup_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_per_step = total_ms / args.steps
+    value = ws * union_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # algorithmic bytes of one moe_verify_dedup call: union expert bytes + the
+    # hidden states (bf16 read, fp16 copy written and read), the
+    # intermediate a (fp16, written and read once per slot) and the per-slot
+    # fp32 outputs (written, read) + y (bf16) + gate weights
+    slots = n * (CFG.top_k + CFG.n_shared)
+    act_bytes = (n * CFG.d * (2 + 2 + 2) + 2 * slots * CFG.inter * 2 + 2 * slots * CFG.d * 4
+                 + n * CFG.d * 2 + n * CFG.top_k * 4)
+    alg_bytes = union_bytes + act_bytes
+    dedup_avg = statistics.mean(dedup_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (dedup_avg * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host h -> device, pass,
+    # y -> pinned host, every step
+    h_host = h.cpu().pin_memory()
+    y_host = torch.empty(n, CFG.d, dtype=torch.bfloat16).pin_memory()
+    h_dev = torch.empty_like(h)
+    for _ in range(3):
+        h_dev.copy_(h_host, non_blocking=True)
+        y = vl.verify_pass(h_dev, n)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(args.steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        y = vl.verify_pass(h_dev, n)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / args.steps
+    e2e_value = ws * union_bytes / (e2e_ms * 1e-3) / 1e9
+
+    sweep = None
+    if not args.no_sweep and rank == 0:
+        sweep = engine_sweep(mv, layer, h_all, args.sweep_max, eb)
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and ws == 1:
+        cpu = cpu_baseline(layer, h, union_bytes)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3 weights x fp16 activations, fp32 accumulate",
+            "data": "synthetic (seeded N(0,0.02^2) weights quantised per 128x128 block; tree hidden states)",
+            "config": {"workload": WORKLOAD, "n_tokens": n, "d": CFG.d, "experts": CFG.n_experts,
+                       "top_k": CFG.top_k, "shared": CFG.n_shared, "inter": CFG.inter,
+                       "U": U, "union_bytes_per_pass": union_bytes,
+                       "l2": "inputs larger than L2 (union bytes per pass >> 129 MB), no flush",
+                       "parallelism": f"replicas x{ws}"},
+            "us_per_pass": round(1e3 * ms_per_step, 2),
+            "us_per_pass_median": round(1e3 * statistics.median(pass_ms), 2),
+            "us_dedup_call": round(1e3 * dedup_avg, 2),
+            "pct_of_nominal_8tbs_whole_pass": round(100 * value / ws / NOMINAL_HBM_GBS, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_kind": peak_kind, "kernel": "moe_verify_dedup (gate/up + down + combine)",
+                         "traffic": traffic_from_profile(),
+                         "algorithmic_bytes_per_launch": alg_bytes},
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": n * CFG.d * 2, "d2h_bytes_per_step": n * CFG.d * 2,
+                    "us_per_pass": round(1e3 * e2e_ms, 2)},
+            "gpu_launches": KERNELS_PER_PASS * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+            "sweep": sweep,
+        }
+        print(json.dumps(out))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def flush_l2(buf_a, buf_b):
+    buf_a.fill_(1)            # write more than L2 ...
+    buf_b.sum()               # ... then read more than L2, so no dirty lines remain
+
+
+def engine_sweep(mv, layer, h_all, n_max, eb, reps=5):
+    """µs per pass of each engine's expert call (after routing and planning,
+    which are shared) for n = 1..n_max, L2 flushed before each timed call."""
+    vl = mv.VerifyLayer(layer, 64)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    a = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    b = torch.ones_like(a)
+    stream = torch.cuda.current_stream()
+    rows = []
+    crossover = None
+    k1 = CFG.top_k + CFG.n_shared
+    for n in range(1, n_max + 1):
+        h = h_all[:n].contiguous()
+        vl.route(h, n)
+        vl.union_plan(n)
+        vl.dedup(h, n)
+        vl.perslot(h, n)
+        torch.cuda.synchronize()
+        U = int(vl.plan.n_uniq[0])
+        t = {}
+        for eng in ("dedup", "perslot"):
+            ts = []
+            for _ in range(reps):
+                flush_l2(a, b)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                (vl.dedup if eng == "dedup" else vl.perslot)(h, n)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            t[eng] = statistics.median(ts)
+        assert vl.last_error() == 0
+        ub = (U + CFG.n_shared) * eb
+        rb = n * k1 * eb
+        u_bar = ub / rb
+        r = (ub / t["dedup"]) / (rb / t["perslot"])
+        rows.append([n, U, round(t["dedup"], 1), round(t["perslot"], 1), round(u_bar, 3),
+                     round(r, 3), round(ub / t["dedup"] / 1e3, 1)])
+        if crossover is None and t["dedup"] < t["perslot"]:
+            crossover = n
+    return {"columns": ["n", "U", "us_dedup", "us_perslot", "u_bar", "r", "gbs_dedup_union"],
+            "rows": rows, "crossover_n": crossover,
+            "l2": "flushed (2x L2 written then 2x L2 read) before each timed call"}
+
+
+# ------------------------------------------------------------- cpu / oracle
+
+def oracle_inputs(layer, h):
+    import numpy as np
+    import oracle
+    cpu = layer.to("cpu")
+
+    def nb(t):
+        if t is None:
+            return None
+        t = t.contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+    L = oracle.Layer(CFG.d, CFG.n_experts, CFG.top_k, CFG.inter, oracle.BF16, oracle.E4M3,
+                     oracle.GATE_SIGMOID_RENORM, nb(cpu.wg), nb(cpu.w13), nb(cpu.w2), nb(cpu.s13),
+                     nb(cpu.s2), nb(cpu.sh_w13), nb(cpu.sh_w2), nb(cpu.sh_s13), nb(cpu.sh_s2))
+    return oracle, L, nb(h.cpu())
+
+
+def cpu_baseline(layer, h, union_bytes, reps=3):
+    """The oracle, as it stands, on all host cores: the whole n-token pass."""
+    oracle, L, hb = oracle_inputs(layer, h)
+    cores = os.cpu_count() or 1
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.verify(L, hb, threads=cores)
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts)
+    return {"value": round(union_bytes / t / 1e9, 4), "unit": "GB/s", "cores": min(cores, N_TOKENS),
+            "kind": "oracle",
+            "sample": f"the whole {N_TOKENS}-token pass (fp64 per-token loop, tokens split over "
+                      f"threads), median of {reps}: {t:.2f} s per pass"}
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    layer, h_all = make_workload(device)
+    h = h_all[:N_TOKENS].contiguous()
+    oracle, L, hb = oracle_inputs(layer, h)
+    cores = os.cpu_count() or 1
+    # union bytes of the pass, from the oracle's own routing
+    hv = h.double().cpu().numpy()
+    U = len({int(e) for t in range(N_TOKENS)
+             for e in oracle.topk(oracle.router_scores(L, hv[t]), CFG.top_k)})
+    wb, sb = oracle.expert_bytes(CFG.d, CFG.inter, oracle.E4M3)
+    union_bytes = (U + CFG.n_shared) * (wb + sb)
+    for _ in range(min(args.warmup, 1)):
+        oracle.verify(L, hb, tokens=[0], threads=1)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.verify(L, hb, threads=cores)
+        ts.append(time.perf_counter() - t0)
+    t = sum(ts) / len(ts)
+    value = union_bytes / t / 1e9
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * t, 1), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeds as ours)",
+           "config": {"workload": WORKLOAD, "n_tokens": N_TOKENS, "U": U,
+                      "union_bytes_per_pass": union_bytes},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": min(cores, N_TOKENS),
+                            "kind": "oracle",
+                            "sample": f"the whole {N_TOKENS}-token pass per step on the host cores"},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

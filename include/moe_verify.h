@@ -1,0 +1,221 @@
+/*
+ * moe_verify.h -- C ABI of the MoE verification-pass library (libmoe_verify.so)
+ *
+ * The library computes the MoE layer of a speculative-decoding verification
+ * pass on one GB300 GPU (sm_103a):
+ *
+ *   1. router scores s = W_g h and top-k selection            (moe_route_topk)
+ *      ("Making Every Verified Token Count: Adaptive Verification for MoE
+ *      Speculative Decoding", Sec. 2.2, eq. (4) and the sentence after it:
+ *      the selected scores are normalised by softmax or sigmoid);
+ *   2. the union of the experts the n tokens select, with a grouping of the
+ *      n*k (token, slot) pairs by expert                        (moe_union_plan)
+ *      (same page, eq. (5); "Less Experts, Faster Decoding: Cost-Aware
+ *      Speculative Decoding for Mixture-of-Experts", eq. (1); "The Limits of
+ *      Speculation: Bounding Speculative Decoding in Mixture-of-Experts",
+ *      App. A.4.1, eqs. (A1)-(A2));
+ *   3. each selected expert's SwiGLU FFN on the tokens routed to it, combined
+ *      with the router weights, by one of two engines
+ *      ("Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
+ *      Kernel Bandwidth and the Best Draft Length", abstract and Fig. 3):
+ *        - deduplicating: every union expert's weights are read from HBM
+ *          once per pass (union bytes U*b)                    (moe_verify_dedup)
+ *        - per-slot: an expert's weights are read once per (token, slot)
+ *          that names it (requested bytes n*k*b)            (moe_verify_perslot)
+ *
+ * Conventions shared by every call
+ *   - Pointers named "device" are CUDA device pointers that the caller
+ *     allocates and owns; the library allocates and frees nothing.
+ *   - Every launching call is asynchronous on `stream` and never synchronises
+ *     the host, so a whole pass can be captured in a CUDA graph.  The one
+ *     exception is moe_last_error(), which synchronises `stream`.
+ *   - Arguments are checked on the host before anything is enqueued; a bad
+ *     argument returns a non-OK status and enqueues nothing.
+ *   - Device arrays must start on a 16-byte boundary.
+ *   - Outputs are fully overwritten.  No C++ exception crosses this ABI.
+ *   - Layout of a layer (row-major everywhere):
+ *       h          [n][d]           act_dtype
+ *       router_w   [N][d]           act_dtype           (W_g; row = expert)
+ *       w13        [N][2I][d]       w_dtype  (rows 0..I-1 gate W1, I..2I-1 up W3)
+ *       w2         [N][d][I]        w_dtype  (down projection)
+ *       s13        [N][2I/128][d/128] float (E4M3 only: block scales)
+ *       s2         [N][d/128][I/128]  float (E4M3 only)
+ *       sh_*       the shared expert, same shapes without the leading N
+ *       y          [n][d]           act_dtype
+ *     An E4M3 weight is q * s where q is the OCP FP8 E4M3 value of the byte
+ *     and s the fp32 scale of its 128 x 128 block.
+ *   - Limits (else MOE_ERR_UNSUPPORTED): N <= 256, 1 <= k <= min(N, 32),
+ *     0 <= n <= n_max <= 64, n_shared 0 or 1, d % 8 == 0; F32 weights go with
+ *     F32 activations and need I % 4 == 0; BF16 and E4M3 weights go with BF16
+ *     activations; BF16 needs d % 64 == 0 and I % 32 == 0, E4M3 needs
+ *     d % 128 == 0 and I % 128 == 0.
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA stream handle (cudaStream_t); 0 is the legacy default stream. */
+typedef void *moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, size out of range, bad enum   */
+  MOE_ERR_UNSUPPORTED = 2, /* a size this build does not handle           */
+  MOE_ERR_ALIGNMENT = 3,   /* a device array not on a 16-byte boundary    */
+  MOE_ERR_WORKSPACE = 4,   /* workspace smaller than moe_workspace_bytes() */
+  MOE_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed        */
+  MOE_ERR_TIMEOUT = 6,     /* a device-side wait hit its time limit       */
+  MOE_ERR_DEVICE_INPUT = 7 /* an expert id read on the device was outside [0, N) */
+} moe_status;
+
+typedef enum {
+  MOE_F32 = 0,      /* IEEE binary32                                     */
+  MOE_BF16 = 1,     /* bfloat16                                          */
+  MOE_E4M3_B128 = 2 /* OCP FP8 E4M3 with one fp32 scale per 128x128 block */
+} moe_dtype;
+
+typedef enum {
+  MOE_GATE_SOFTMAX = 0,        /* softmax over all N scores; keep the k selected  */
+  MOE_GATE_SOFTMAX_RENORM = 1, /* softmax over the k selected scores              */
+  MOE_GATE_SIGMOID_RENORM = 2  /* sigmoid of the k selected scores / their sum    */
+} moe_gate;
+
+typedef struct {
+  int32_t d;               /* hidden size                                 */
+  int32_t n_experts;       /* routed experts N                            */
+  int32_t top_k;           /* experts per token k                         */
+  int32_t inter;           /* SwiGLU intermediate size I                  */
+  int32_t n_shared;        /* 0 or 1 shared expert, applied with weight 1 */
+  int32_t n_max;           /* largest n any call with this desc will pass */
+  int32_t act_dtype;       /* MOE_F32 or MOE_BF16 (h, router_w, y)        */
+  int32_t w_dtype;         /* moe_dtype of the expert weights             */
+  int32_t gate;            /* moe_gate                                    */
+  int32_t wait_timeout_us; /* limit of every device-side wait; 0 = 1 s    */
+} moe_layer_desc;
+
+typedef struct {
+  const void *w13;    /* device, [N][2I][d]                         */
+  const void *w2;     /* device, [N][d][I]                          */
+  const float *s13;   /* device, E4M3 only, else NULL               */
+  const float *s2;    /* device, E4M3 only, else NULL               */
+  const void *sh_w13; /* device, shared expert [2I][d]; NULL if none */
+  const void *sh_w2;  /* device, shared expert [d][I]                */
+  const float *sh_s13;
+  const float *sh_s2;
+} moe_expert_weights;
+
+/* The union plan (all device arrays, owned by the caller). */
+typedef struct {
+  int32_t *hist;        /* [N]     slots that name each expert                */
+  int32_t *uniq;        /* [N]     the U distinct experts, ascending; the
+                                   entries from U on are left unspecified     */
+  int32_t *n_uniq;      /* [1]     U                                          */
+  int32_t *offs;        /* [N+1]   group u of perm is offs[u] .. offs[u+1]-1;
+                                   offs[U] = n*k; later entries unspecified   */
+  int32_t *perm;        /* [n_max*k] slot indices t*k+j grouped by expert in
+                                   uniq order, ascending inside a group       */
+  int64_t *union_bytes; /* [1]     (U + n_shared) * (expert weight bytes +
+                                   expert scale bytes)                        */
+} moe_plan;
+
+/* Bytes of the caller-owned workspace that moe_verify_dedup and
+ * moe_verify_perslot need for this desc (sized for desc->n_max).  Returns 0
+ * for an invalid desc. */
+size_t moe_workspace_bytes(const moe_layer_desc *desc);
+
+/* Bytes of one expert: its three matrices (*weight_bytes = 3*d*I*element
+ * size) and, for E4M3, its fp32 block scales (*scale_bytes).  Either
+ * pointer may be NULL. */
+moe_status moe_expert_bytes(const moe_layer_desc *desc, int64_t *weight_bytes,
+                            int64_t *scale_bytes);
+
+/* Router scores and top-k ("Making Every Verified Token Count", Sec. 2.2,
+ * eq. (4)).  For each of the n tokens: logits[t][e] = sum_i router_w[e][i] *
+ * h[t][i] accumulated in fp32; ids[t][0..k) = the k experts with the largest
+ * logits, largest first, equal logits ordered by lower id; w[t][j] = the
+ * gate weight of ids[t][j] (desc->gate).
+ *   router_w  device [N][d] act_dtype;   h  device [n][d] act_dtype
+ *   ids       device [n][k] int32 (out); w  device [n][k] float (out)
+ *   logits    device [n][N] float (out; required: the scores are staged
+ *             there between the two kernels)
+ * n may be 0 (nothing is enqueued). */
+moe_status moe_route_topk(const moe_layer_desc *desc, const void *router_w,
+                          const void *h, int32_t n, int32_t *ids, float *w,
+                          float *logits, moe_stream_t stream);
+
+/* The top-k and gate stage of moe_route_topk on given fp32 logits
+ * (device [n][N]).  Its ids equal a full sort of each row by (logit
+ * descending, id ascending), bit for bit. */
+moe_status moe_topk_from_logits(const moe_layer_desc *desc,
+                                const float *logits, int32_t n, int32_t *ids,
+                                float *w, moe_stream_t stream);
+
+/* The expert union of the routed ids (device [n][k] int32) and the grouping
+ * of the n*k slots by expert, written to `plan` (see moe_plan).  An id
+ * outside [0, N) is left out of the plan and makes moe_last_error() report
+ * MOE_ERR_DEVICE_INPUT when `error_word` is not NULL.
+ *   error_word  device int32 that receives the first device-side error, or
+ *               NULL; the workspace of moe_verify_* starts with such a word. */
+moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids,
+                          int32_t n, const moe_plan *plan, int32_t *error_word,
+                          moe_stream_t stream);
+
+/* The layer output with the deduplicating engine: every expert of the plan
+ * (plus the shared expert) is applied once to all tokens routed to it, its
+ * weights streamed from HBM once per pass, and
+ *   y[t] = sum_j w[t][j] * FFN_{ids[t][j]}(h[t]) (+ FFN_shared(h[t])),
+ * summed in the fixed order j = 0..k-1, then the shared expert.
+ *   weights    the layer's experts (device pointers inside)
+ *   h          device [n][d] act_dtype;   ids  device [n][k] int32
+ *   w          device [n][k] float;       plan built by moe_union_plan from ids
+ *   workspace  device, ws_bytes >= moe_workspace_bytes(desc)
+ *   y          device [n][d] act_dtype (out)
+ * The intermediate activations are kept in fp32 (F32 weights), bf16 (BF16
+ * weights) or fp16 (E4M3 weights, whose values are exact in fp16). */
+moe_status moe_verify_dedup(const moe_layer_desc *desc,
+                            const moe_expert_weights *weights, const void *h,
+                            int32_t n, const int32_t *ids, const float *w,
+                            const moe_plan *plan, void *workspace,
+                            size_t ws_bytes, void *y, moe_stream_t stream);
+
+/* The same output with the per-slot engine: each (token, slot) pair, and
+ * each token's shared-expert slot, runs its expert's FFN for that one token,
+ * reading the expert's weights once per pair.  No plan is needed. */
+moe_status moe_verify_perslot(const moe_layer_desc *desc,
+                              const moe_expert_weights *weights,
+                              const void *h, int32_t n, const int32_t *ids,
+                              const float *w, void *workspace, size_t ws_bytes,
+                              void *y, moe_stream_t stream);
+
+/* Zeroes the error word at the start of a fresh workspace (enqueued on
+ * `stream`).  Call once after allocating a workspace; moe_last_error() clears
+ * the word again after reading it. */
+moe_status moe_workspace_init(void *workspace, size_t ws_bytes,
+                              moe_stream_t stream);
+
+/* Synchronises `stream`, then returns (and clears) the first error that a
+ * kernel recorded in the workspace's error word: MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE_INPUT; MOE_ERR_CUDA if the synchronisation itself failed. */
+moe_status moe_last_error(void *workspace, moe_stream_t stream);
+
+/* Self-test of the device-side bounded wait used by every kernel: launches
+ * one CTA that waits on a barrier nothing ever arrives on, gives up after
+ * limit_us microseconds (1 <= limit_us <= 1000000), records MOE_ERR_TIMEOUT
+ * in *error_word (device int32) and returns, leaving the context usable. */
+moe_status moe_selftest_bounded_wait(int32_t *error_word, int32_t limit_us,
+                                     moe_stream_t stream);
+
+/* A short English description of a status code (static storage). */
+const char *moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

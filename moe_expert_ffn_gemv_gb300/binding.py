@@ -1,0 +1,274 @@
+"""Python binding of libmoe_verify.so (include/moe_verify.h).
+
+Argument marshalling only: every step of the verification pass runs in the
+library's CUDA kernels.  PyTorch provides device memory and the current CUDA
+stream.  Importing this module loads the library and raises if it is missing
+(build it with ``python -m moe_expert_ffn_gemv_gb300.build``): there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import synth
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_verify.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m moe_expert_ffn_gemv_gb300.build` "
+                      "(needs the CUDA toolkit); there is no CPU fallback")
+_lib = ctypes.CDLL(LIB_PATH)
+
+# status codes, dtypes and gates as numbered in include/moe_verify.h
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_ALIGNMENT = 0, 1, 2, 3
+MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_INPUT = 4, 5, 6, 7
+MOE_F32, MOE_BF16, MOE_E4M3_B128 = 0, 1, 2
+MOE_GATE_SOFTMAX, MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1, 2
+
+EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_topk_from_logits",
+            "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot", "moe_workspace_init",
+            "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string"]
+
+
+class moe_layer_desc(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int32) for f in
+                ("d", "n_experts", "top_k", "inter", "n_shared", "n_max", "act_dtype", "w_dtype",
+                 "gate", "wait_timeout_us")]
+
+
+class moe_expert_weights(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in
+                ("w13", "w2", "s13", "s2", "sh_w13", "sh_w2", "sh_s13", "sh_s2")]
+
+
+class moe_plan(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in
+                ("hist", "uniq", "n_uniq", "offs", "perm", "union_bytes")]
+
+
+_P = ctypes.c_void_p
+_D = ctypes.POINTER(moe_layer_desc)
+_lib.moe_workspace_bytes.restype = ctypes.c_size_t
+_lib.moe_workspace_bytes.argtypes = [_D]
+_lib.moe_expert_bytes.restype = ctypes.c_int
+_lib.moe_expert_bytes.argtypes = [_D, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
+_lib.moe_route_topk.restype = ctypes.c_int
+_lib.moe_route_topk.argtypes = [_D, _P, _P, ctypes.c_int32, _P, _P, _P, _P]
+_lib.moe_topk_from_logits.restype = ctypes.c_int
+_lib.moe_topk_from_logits.argtypes = [_D, _P, ctypes.c_int32, _P, _P, _P]
+_lib.moe_union_plan.restype = ctypes.c_int
+_lib.moe_union_plan.argtypes = [_D, _P, ctypes.c_int32, ctypes.POINTER(moe_plan), _P, _P]
+_lib.moe_verify_dedup.restype = ctypes.c_int
+_lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32, _P,
+                                  _P, ctypes.POINTER(moe_plan), _P, ctypes.c_size_t, _P, _P]
+_lib.moe_verify_perslot.restype = ctypes.c_int
+_lib.moe_verify_perslot.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32,
+                                    _P, _P, _P, ctypes.c_size_t, _P, _P]
+_lib.moe_workspace_init.restype = ctypes.c_int
+_lib.moe_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
+_lib.moe_last_error.restype = ctypes.c_int
+_lib.moe_last_error.argtypes = [_P, _P]
+_lib.moe_selftest_bounded_wait.restype = ctypes.c_int
+_lib.moe_selftest_bounded_wait.argtypes = [_P, ctypes.c_int32, _P]
+_lib.moe_status_string.restype = ctypes.c_char_p
+_lib.moe_status_string.argtypes = [ctypes.c_int]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {moe_status_string(status)} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------- the C calls
+
+def moe_status_string(status: int) -> str:
+    return _lib.moe_status_string(status).decode()
+
+
+def moe_workspace_bytes(desc: moe_layer_desc) -> int:
+    return int(_lib.moe_workspace_bytes(ctypes.byref(desc)))
+
+
+def moe_expert_bytes(desc: moe_layer_desc):
+    wb, sb = ctypes.c_int64(), ctypes.c_int64()
+    _check(_lib.moe_expert_bytes(ctypes.byref(desc), ctypes.byref(wb), ctypes.byref(sb)),
+           "moe_expert_bytes")
+    return wb.value, sb.value
+
+
+def moe_route_topk(desc, router_w, h, n, ids, w, logits, stream=None) -> None:
+    _check(_lib.moe_route_topk(ctypes.byref(desc), _ptr(router_w), _ptr(h), n, _ptr(ids), _ptr(w),
+                               _ptr(logits), _stream(stream)), "moe_route_topk")
+
+
+def moe_topk_from_logits(desc, logits, n, ids, w, stream=None) -> None:
+    _check(_lib.moe_topk_from_logits(ctypes.byref(desc), _ptr(logits), n, _ptr(ids), _ptr(w),
+                                     _stream(stream)), "moe_topk_from_logits")
+
+
+def moe_union_plan(desc, ids, n, plan: moe_plan, error_word=None, stream=None) -> None:
+    _check(_lib.moe_union_plan(ctypes.byref(desc), _ptr(ids), n, ctypes.byref(plan),
+                               _ptr(error_word), _stream(stream)), "moe_union_plan")
+
+
+def moe_verify_dedup(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_plan, workspace,
+                     y, stream=None) -> None:
+    _check(_lib.moe_verify_dedup(ctypes.byref(desc), ctypes.byref(weights), _ptr(h), n, _ptr(ids),
+                                 _ptr(w), ctypes.byref(plan), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(y),
+                                 _stream(stream)), "moe_verify_dedup")
+
+
+def moe_verify_perslot(desc, weights: moe_expert_weights, h, n, ids, w, workspace, y,
+                       stream=None) -> None:
+    _check(_lib.moe_verify_perslot(ctypes.byref(desc), ctypes.byref(weights), _ptr(h), n,
+                                   _ptr(ids), _ptr(w), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(y),
+                                   _stream(stream)), "moe_verify_perslot")
+
+
+def moe_workspace_init(workspace, stream=None) -> None:
+    _check(_lib.moe_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "moe_workspace_init")
+
+
+def moe_last_error(workspace, stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device error word."""
+    return int(_lib.moe_last_error(_ptr(workspace), _stream(stream)))
+
+
+def moe_selftest_bounded_wait(error_word, limit_us: int, stream=None) -> None:
+    _check(_lib.moe_selftest_bounded_wait(_ptr(error_word), limit_us, _stream(stream)),
+           "moe_selftest_bounded_wait")
+
+
+# ------------------------------------------------------- layer convenience
+
+_DT = {synth.F32: MOE_F32, synth.BF16: MOE_BF16, synth.E4M3: MOE_E4M3_B128}
+_GATE = {synth.GATE_SOFTMAX: MOE_GATE_SOFTMAX, synth.GATE_SOFTMAX_RENORM: MOE_GATE_SOFTMAX_RENORM,
+         synth.GATE_SIGMOID_RENORM: MOE_GATE_SIGMOID_RENORM}
+
+
+def make_desc(cfg: synth.LayerConfig, n_max: int, wait_timeout_us: int = 0) -> moe_layer_desc:
+    return moe_layer_desc(cfg.d, cfg.n_experts, cfg.top_k, cfg.inter, cfg.n_shared, n_max,
+                          _DT[cfg.act], _DT[cfg.wtype], _GATE[cfg.gate], wait_timeout_us)
+
+
+def make_weights(layer: synth.Layer) -> moe_expert_weights:
+    return moe_expert_weights(_ptr(layer.w13), _ptr(layer.w2), _ptr(layer.s13), _ptr(layer.s2),
+                              _ptr(layer.sh_w13), _ptr(layer.sh_w2), _ptr(layer.sh_s13),
+                              _ptr(layer.sh_s2))
+
+
+@dataclass
+class PlanBuffers:
+    hist: torch.Tensor
+    uniq: torch.Tensor
+    n_uniq: torch.Tensor
+    offs: torch.Tensor
+    perm: torch.Tensor
+    union_bytes: torch.Tensor
+
+    def c(self) -> moe_plan:
+        return moe_plan(*(_ptr(t) for t in (self.hist, self.uniq, self.n_uniq, self.offs,
+                                            self.perm, self.union_bytes)))
+
+
+def _aligned_empty(count: int, dtype, device) -> torch.Tensor:
+    # torch allocations start on 512-byte boundaries; keep each array separate
+    return torch.empty(max(count, 4), dtype=dtype, device=device)
+
+
+class VerifyLayer:
+    """Device buffers of one layer and the calls of one verification pass.
+
+    Owns nothing but torch tensors; every method is one or more C calls on the
+    current stream.  `weights` must stay alive as long as this object.
+    """
+
+    def __init__(self, layer: synth.Layer, n_max: int, device="cuda", wait_timeout_us: int = 0):
+        cfg = layer.cfg
+        self.layer = layer
+        self.cfg = cfg
+        self.n_max = n_max
+        self.desc = make_desc(cfg, n_max, wait_timeout_us)
+        self.weights = make_weights(layer)
+        nb = moe_workspace_bytes(self.desc)
+        if nb == 0:
+            raise MoeError(MOE_ERR_UNSUPPORTED, "moe_workspace_bytes")
+        self.workspace = torch.empty(nb, dtype=torch.uint8, device=device)
+        moe_workspace_init(self.workspace)
+        k, E = cfg.top_k, cfg.n_experts
+        i32 = torch.int32
+        self.ids = _aligned_empty(n_max * k, i32, device)
+        self.w = _aligned_empty(n_max * k, torch.float32, device)
+        self.logits = _aligned_empty(n_max * E, torch.float32, device)
+        self.plan = PlanBuffers(_aligned_empty(E, i32, device), _aligned_empty(E, i32, device),
+                                _aligned_empty(1, i32, device), _aligned_empty(E + 1, i32, device),
+                                _aligned_empty(n_max * k, i32, device),
+                                _aligned_empty(1, torch.int64, device))
+        self._cplan = self.plan.c()
+        self.error_word = self.workspace[:4].view(torch.int32)
+        self.y = torch.empty(n_max, cfg.d, dtype=synth.torch_dtype(cfg.act), device=device)
+
+    def route(self, h: torch.Tensor, n: int) -> None:
+        moe_route_topk(self.desc, self.layer.wg, h, n, self.ids, self.w, self.logits)
+
+    def union_plan(self, n: int) -> None:
+        moe_union_plan(self.desc, self.ids, n, self._cplan, self.error_word)
+
+    def dedup(self, h: torch.Tensor, n: int, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+        y = self.y if y is None else y
+        moe_verify_dedup(self.desc, self.weights, h, n, self.ids, self.w, self._cplan,
+                         self.workspace, y)
+        return y[:n]
+
+    def perslot(self, h: torch.Tensor, n: int, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+        y = self.y if y is None else y
+        moe_verify_perslot(self.desc, self.weights, h, n, self.ids, self.w, self.workspace, y)
+        return y[:n]
+
+    def verify_pass(self, h: torch.Tensor, n: int, engine: str = "dedup",
+                    y: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Route, plan and run the experts: one MoE verification pass."""
+        self.route(h, n)
+        if engine == "dedup":
+            self.union_plan(n)
+            return self.dedup(h, n, y)
+        return self.perslot(h, n, y)
+
+    def last_error(self) -> int:
+        return moe_last_error(self.workspace)
+
+    # views of the routing results
+    def ids_view(self, n):
+        return self.ids[:n * self.cfg.top_k].view(n, self.cfg.top_k)
+
+    def w_view(self, n):
+        return self.w[:n * self.cfg.top_k].view(n, self.cfg.top_k)
+
+    def logits_view(self, n):
+        return self.logits[:n * self.cfg.n_experts].view(n, self.cfg.n_experts)

@@ -1,0 +1,346 @@
+// api.cu -- the C ABI (include/moe_verify.h): argument checks on the host,
+// then the launches of one verification pass on the caller's stream.
+// Nothing here allocates device memory or synchronises the host, except
+// moe_last_error().
+#include <stdint.h>
+#include <string.h>
+
+#include "kernels.h"
+#include "moe_common.cuh"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+namespace {
+
+constexpr int MAX_EXPERTS = 256;
+constexpr int MAX_TOPK = 32;
+constexpr int MAX_TOKENS = 64;
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000ull * 1000 * 1000;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_desc(const moe_layer_desc *L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (L->d <= 0 || L->n_experts <= 0 || L->top_k <= 0 || L->inter <= 0 || L->n_max <= 0 ||
+      L->n_shared < 0 || L->wait_timeout_us < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (L->top_k > L->n_experts) return MOE_ERR_INVALID_ARG;
+  if (L->act_dtype != MOE_F32 && L->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (L->w_dtype != MOE_F32 && L->w_dtype != MOE_BF16 && L->w_dtype != MOE_E4M3_B128)
+    return MOE_ERR_INVALID_ARG;
+  if (L->gate != MOE_GATE_SOFTMAX && L->gate != MOE_GATE_SOFTMAX_RENORM &&
+      L->gate != MOE_GATE_SIGMOID_RENORM)
+    return MOE_ERR_INVALID_ARG;
+  if (L->n_experts > MAX_EXPERTS || L->top_k > MAX_TOPK || L->n_max > MAX_TOKENS ||
+      L->n_shared > 1)
+    return MOE_ERR_UNSUPPORTED;
+  // fp32 weights go with fp32 activations; bf16/E4M3 weights with bf16 ones
+  if ((L->w_dtype == MOE_F32) != (L->act_dtype == MOE_F32)) return MOE_ERR_UNSUPPORTED;
+  if (L->d % 8) return MOE_ERR_UNSUPPORTED;
+  switch (L->w_dtype) {
+    case MOE_F32:
+      if (L->inter % 4) return MOE_ERR_UNSUPPORTED;
+      break;
+    case MOE_BF16:
+      if (L->d % 64 || L->inter % 32) return MOE_ERR_UNSUPPORTED;
+      break;
+    default:
+      if (L->d % 128 || L->inter % 128) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+size_t w_size(const moe_layer_desc &L) {
+  return L.w_dtype == MOE_F32 ? 4 : L.w_dtype == MOE_BF16 ? 2 : 1;
+}
+
+void expert_bytes(const moe_layer_desc &L, int64_t *wb, int64_t *sb) {
+  *wb = int64_t(3) * L.d * L.inter * int64_t(w_size(L));
+  *sb = 0;
+  if (L.w_dtype == MOE_E4M3_B128)
+    *sb = int64_t(4) * ((int64_t(2) * L.inter / 128) * (L.d / 128) +
+                        (int64_t(L.d) / 128) * (L.inter / 128));
+}
+
+uint64_t timeout_ns(const moe_layer_desc &L) {
+  return L.wait_timeout_us > 0 ? uint64_t(L.wait_timeout_us) * 1000ull : DEFAULT_TIMEOUT_NS;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_weights(const moe_layer_desc &L, const moe_expert_weights *W) {
+  if (!W || !W->w13 || !W->w2) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W->w13) || !aligned16(W->w2)) return MOE_ERR_ALIGNMENT;
+  const bool fp8 = L.w_dtype == MOE_E4M3_B128;
+  if (fp8 && (!W->s13 || !W->s2)) return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!aligned16(W->s13) || !aligned16(W->s2))) return MOE_ERR_ALIGNMENT;
+  if (L.n_shared) {
+    if (!W->sh_w13 || !W->sh_w2) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(W->sh_w13) || !aligned16(W->sh_w2)) return MOE_ERR_ALIGNMENT;
+    if (fp8 && (!W->sh_s13 || !W->sh_s2)) return MOE_ERR_INVALID_ARG;
+    if (fp8 && (!aligned16(W->sh_s13) || !aligned16(W->sh_s2))) return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+// The expert FFN of one pass (both phases) and the combine, for either engine.
+moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, const void *h, int n,
+                       const int32_t *ids, const float *w, const moe_plan *plan, void *workspace,
+                       void *y, cudaStream_t stream) {
+  const Workspace ws = workspace_layout(L);
+  uint8_t *wsb = static_cast<uint8_t *>(workspace);
+  int32_t *err = reinterpret_cast<int32_t *>(wsb);
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+
+  SegTables T;
+  memset(&T, 0, sizeof T);
+  T.ids = ids;
+  T.n = n;
+  T.k = L.top_k;
+  T.n_experts = L.n_experts;
+  T.n_shared = L.n_shared;
+  T.dedup = plan != nullptr;
+  if (plan) {
+    T.uniq = plan->uniq;
+    T.offs = plan->offs;
+    T.perm = plan->perm;
+    T.n_uniq = plan->n_uniq;
+  }
+  cudaError_t e = cudaSuccess;
+  if (L.w_dtype == MOE_F32) {
+    F32Params P;
+    P.T = T;
+    P.w13 = static_cast<const float *>(W.w13);
+    P.w2 = static_cast<const float *>(W.w2);
+    P.sh_w13 = static_cast<const float *>(W.sh_w13);
+    P.sh_w2 = static_cast<const float *>(W.sh_w2);
+    P.d = L.d;
+    P.inter = L.inter;
+    P.h = static_cast<const float *>(h);
+    P.inter_out = reinterpret_cast<float *>(wsb + ws.inter);
+    P.yslot = reinterpret_cast<float *>(wsb + ws.yslot);
+    P.err = err;
+    e = launch_expert_f32(1, P, 2 * sms, stream);
+    if (e == cudaSuccess) e = launch_expert_f32(2, P, 2 * sms, stream);
+  } else {
+    const bool fp8 = L.w_dtype == MOE_E4M3_B128;
+    const void *act = h;
+    if (fp8) {
+      e = launch_bf16_to_f16(h, wsb + ws.act16, int64_t(n) * L.d, stream);
+      act = wsb + ws.act16;
+    }
+    // tokens per segment: at most n (dedup; one per slot for per-slot)
+    const int m_max = plan ? n : 1;
+    const int n_tiles = m_max <= 8 ? 1 : m_max <= 16 ? 2 : 4;
+    TcParams P;
+    P.T = T;
+    P.err = err;
+    P.timeout_ns = timeout_ns(L);
+    P.inter = L.inter;
+    const size_t es = w_size(L);
+    // phase 1: gate/up over W13, K = d
+    P.w = static_cast<const uint8_t *>(W.w13);
+    P.w_sh = static_cast<const uint8_t *>(W.sh_w13);
+    P.sc = W.s13;
+    P.sc_sh = W.sh_s13;
+    P.expert_stride = int64_t(2) * L.inter * L.d * int64_t(es);
+    P.rows_total = 2 * L.inter;
+    P.kdim = L.d;
+    P.row_blocks = L.inter / 32;
+    P.act = act;
+    P.out = wsb + ws.inter;
+    if (e == cudaSuccess) e = launch_expert_tc(fp8, 1, n_tiles, P, sms, stream);
+    // phase 2: down over W2, K = I
+    P.w = static_cast<const uint8_t *>(W.w2);
+    P.w_sh = static_cast<const uint8_t *>(W.sh_w2);
+    P.sc = W.s2;
+    P.sc_sh = W.sh_s2;
+    P.expert_stride = int64_t(L.d) * L.inter * int64_t(es);
+    P.rows_total = L.d;
+    P.kdim = L.inter;
+    P.row_blocks = L.d / 64;
+    P.act = wsb + ws.inter;
+    P.out = wsb + ws.yslot;
+    if (e == cudaSuccess) e = launch_expert_tc(fp8, 2, n_tiles, P, sms, stream);
+  }
+  if (e == cudaSuccess)
+    e = launch_combine(reinterpret_cast<const float *>(wsb + ws.yslot), w, n, L.top_k, L.d,
+                       L.n_shared, L.act_dtype == MOE_BF16, y, stream);
+  return cuda_status(e);
+}
+
+moe_status check_verify_args(const moe_layer_desc *desc, const moe_expert_weights *weights,
+                             const void *h, int32_t n, const int32_t *ids, const float *w,
+                             void *workspace, size_t ws_bytes, void *y) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  s = check_weights(*desc, weights);
+  if (s != MOE_OK) return s;
+  if (!h || !ids || !w || !workspace || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(ids) || !aligned16(w) || !aligned16(workspace) ||
+      !aligned16(y))
+    return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < workspace_layout(*desc).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// Waits on a barrier that nothing arrives on; the wait must give up.
+__global__ void bounded_wait_selftest_kernel(int32_t *err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool done = mbar_wait_bounded(&bar, 0, limit_ns);
+  if (!done && threadIdx.x == 0) record_error(err, MOE_ERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status moe_selftest_bounded_wait(int32_t *error_word, int32_t limit_us,
+                                             moe_stream_t stream) {
+  if (!error_word || limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      error_word, uint64_t(limit_us) * 1000ull);
+  return cuda_status(cudaGetLastError());
+}
+
+MOE_API size_t moe_workspace_bytes(const moe_layer_desc *desc) {
+  if (check_desc(desc) != MOE_OK) return 0;
+  return workspace_layout(*desc).total;
+}
+
+MOE_API moe_status moe_expert_bytes(const moe_layer_desc *desc, int64_t *weight_bytes,
+                                    int64_t *scale_bytes) {
+  const moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  int64_t wb, sb;
+  expert_bytes(*desc, &wb, &sb);
+  if (weight_bytes) *weight_bytes = wb;
+  if (scale_bytes) *scale_bytes = sb;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_route_topk(const moe_layer_desc *desc, const void *router_w, const void *h,
+                                  int32_t n, int32_t *ids, float *w, float *logits,
+                                  moe_stream_t stream) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (!router_w || !h || !ids || !w || !logits) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(router_w) || !aligned16(h) || !aligned16(ids) || !aligned16(w) ||
+      !aligned16(logits))
+    return MOE_ERR_ALIGNMENT;
+  if (n == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_router_scores(desc->act_dtype == MOE_BF16, router_w, h, n, desc->d,
+                                       desc->n_experts, logits, st);
+  if (e == cudaSuccess)
+    e = launch_topk_gate(logits, n, desc->n_experts, desc->top_k, desc->gate, ids, w, st);
+  return cuda_status(e);
+}
+
+MOE_API moe_status moe_topk_from_logits(const moe_layer_desc *desc, const float *logits,
+                                        int32_t n, int32_t *ids, float *w, moe_stream_t stream) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (!logits || !ids || !w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(ids) || !aligned16(w)) return MOE_ERR_ALIGNMENT;
+  if (n == 0) return MOE_OK;
+  return cuda_status(launch_topk_gate(logits, n, desc->n_experts, desc->top_k, desc->gate, ids, w,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids, int32_t n,
+                                  const moe_plan *plan, int32_t *error_word,
+                                  moe_stream_t stream) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (!plan || !plan->hist || !plan->uniq || !plan->n_uniq || !plan->offs || !plan->perm ||
+      !plan->union_bytes || (n > 0 && !ids))
+    return MOE_ERR_INVALID_ARG;
+  if ((ids && !aligned16(ids)) || !aligned16(plan->hist) || !aligned16(plan->uniq) ||
+      !aligned16(plan->offs) || !aligned16(plan->perm))
+    return MOE_ERR_ALIGNMENT;
+  int64_t wb, sb;
+  expert_bytes(*desc, &wb, &sb);
+  return cuda_status(launch_union_plan(ids, n * desc->top_k, desc->n_experts, desc->n_shared,
+                                       wb + sb, plan->hist, plan->uniq, plan->n_uniq, plan->offs,
+                                       plan->perm, plan->union_bytes, error_word,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API moe_status moe_verify_dedup(const moe_layer_desc *desc, const moe_expert_weights *weights,
+                                    const void *h, int32_t n, const int32_t *ids, const float *w,
+                                    const moe_plan *plan, void *workspace, size_t ws_bytes,
+                                    void *y, moe_stream_t stream) {
+  moe_status s = check_verify_args(desc, weights, h, n, ids, w, workspace, ws_bytes, y);
+  if (s != MOE_OK) return s;
+  if (!plan || !plan->uniq || !plan->offs || !plan->perm || !plan->n_uniq)
+    return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  return run_experts(*desc, *weights, h, n, ids, w, plan, workspace, y,
+                     static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_verify_perslot(const moe_layer_desc *desc,
+                                      const moe_expert_weights *weights, const void *h, int32_t n,
+                                      const int32_t *ids, const float *w, void *workspace,
+                                      size_t ws_bytes, void *y, moe_stream_t stream) {
+  moe_status s = check_verify_args(desc, weights, h, n, ids, w, workspace, ws_bytes, y);
+  if (s != MOE_OK) return s;
+  if (n == 0) return MOE_OK;
+  return run_experts(*desc, *weights, h, n, ids, w, nullptr, workspace, y,
+                     static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_workspace_init(void *workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (!workspace || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return MOE_ERR_ALIGNMENT;
+  return cuda_status(cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API moe_status moe_last_error(void *workspace, moe_stream_t stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof word) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(word);
+}
+
+MOE_API const char *moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or type combination";
+    case MOE_ERR_ALIGNMENT: return "device array not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_INPUT: return "expert id out of range on the device";
+  }
+  return "unknown status";
+}

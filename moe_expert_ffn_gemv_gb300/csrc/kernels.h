@@ -1,0 +1,68 @@
+// kernels.h -- launchers of the library's kernels (internal; C++ linkage).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// Parameters of one launch of the tensor-core expert kernel (expert_tc.cu).
+struct TcParams {
+  SegTables T;
+  const uint8_t *w;       // routed experts' matrix (W13 or W2), expert-major
+  const uint8_t *w_sh;    // the shared expert's matrix, or null
+  const float *sc;        // E4M3 block scales of `w` ([N][rows/128][kdim/128])
+  const float *sc_sh;     // E4M3 block scales of `w_sh`
+  int64_t expert_stride;  // bytes between consecutive experts in `w`
+  int32_t rows_total;     // rows of one expert's matrix: 2I (phase 1) or d (phase 2)
+  int32_t kdim;           // columns: d (phase 1) or I (phase 2)
+  int32_t inter;          // I
+  int32_t row_blocks;     // work items per segment: I/32 (phase 1) or d/64 (phase 2)
+  const void *act;        // phase 1: activations [n][d] by token; phase 2: a [slots][I]
+  void *out;              // phase 1: a [slots][I]; phase 2: yslot [slots][d] fp32
+  int32_t *err;           // workspace error word
+  uint64_t timeout_ns;    // limit of every wait
+};
+
+// Tensor-core expert FFN (BF16 weights, or E4M3 with fp32 block scales);
+// n_tiles = 8-token MMA tiles per pass (1, 2 or 4).
+cudaError_t launch_expert_tc(bool fp8, int phase, int n_tiles, const TcParams &P, int grid,
+                             cudaStream_t stream);
+
+// FP32 expert FFN on CUDA cores (same segment tables, same outputs).
+struct F32Params {
+  SegTables T;
+  const float *w13, *w2;        // routed experts
+  const float *sh_w13, *sh_w2;  // shared expert (or null)
+  int32_t d, inter;
+  const float *h;               // [n][d]
+  float *inter_out;             // [slots][I]
+  float *yslot;                 // [slots][d]
+  int32_t *err;
+};
+cudaError_t launch_expert_f32(int phase, const F32Params &P, int grid, cudaStream_t stream);
+
+// Router scores logits[t][e] = W_g[e] . h[t] (fp32 accumulation).
+cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h, int n, int d,
+                                 int n_experts, float *logits, cudaStream_t stream);
+
+// Top-k (largest first, ties to the lower id) and gate weights per token.
+cudaError_t launch_topk_gate(const float *logits, int n, int n_experts, int k, int gate,
+                             int32_t *ids, float *w, cudaStream_t stream);
+
+// Expert union and slot permutation (one CTA).
+cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, int n_shared,
+                              int64_t expert_bytes, int32_t *hist, int32_t *uniq, int32_t *n_uniq,
+                              int32_t *offs, int32_t *perm, int64_t *union_bytes, int32_t *err,
+                              cudaStream_t stream);
+
+// bf16 -> fp16 copy of the hidden states (E4M3 path).
+cudaError_t launch_bf16_to_f16(const void *src, void *dst, int64_t count, cudaStream_t stream);
+
+// y[t] = sum_j w[t][j] yslot[t*k+j] (+ yslot[n*k+t]) -> y (fp32 or bf16).
+cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,
+                           bool out_bf16, void *y, cudaStream_t stream);
+
+}  // namespace moe

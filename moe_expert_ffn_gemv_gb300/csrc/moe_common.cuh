@@ -1,0 +1,225 @@
+// moe_common.cuh -- device helpers shared by the library's kernels:
+// mbarrier and bulk-copy (TMA) wrappers in inline PTX, bounded waits, error
+// recording and the workspace layout.  Internal to the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_verify.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ status
+
+// The first device-side error wins; later ones are dropped.
+__device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with parity `parity` to complete, for at most
+// `limit_ns` nanoseconds.  Returns false on time-out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return mbar_try_wait(bar, parity);
+  }
+}
+
+// ------------------------------------------------------------- bulk copies
+
+// L2 policy for data read exactly once (expert weights): evict first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// One-dimensional TMA bulk copy global -> shared, completing `bytes` of
+// transaction count on `bar`.  dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------ tensor cores
+
+// D += A * B for one m16n8k16 tile, f16 or bf16 inputs, fp32 accumulators.
+template <bool BF16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
+                                          uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// Two E4M3 bytes (low byte first) -> f16x2 (low half = low byte); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// --------------------------------------------------------------- workspace
+
+// Layout of the caller's workspace (all offsets 256-byte aligned):
+//   [0, 256)           int32 error word (+ padding)
+//   act16              [n_max][d] fp16 copy of h (E4M3 weights only)
+//   inter              [n_max*(k+n_shared)][I] intermediate a = silu(g)*u
+//   yslot              [n_max*(k+n_shared)][d] fp32 per-slot expert outputs
+struct Workspace {
+  size_t act16, inter, yslot, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline Workspace workspace_layout(const moe_layer_desc &L) {
+  const size_t slots = size_t(L.n_max) * size_t(L.top_k + L.n_shared);
+  const size_t inter_es = L.w_dtype == MOE_F32 ? 4 : 2;
+  Workspace w;
+  size_t off = 256;
+  w.act16 = off;
+  off += align256(L.w_dtype == MOE_E4M3_B128 ? size_t(L.n_max) * L.d * 2 : 0);
+  w.inter = off;
+  off += align256(slots * size_t(L.inter) * inter_es);
+  w.yslot = off;
+  off += align256(slots * size_t(L.d) * 4);
+  w.total = off;
+  return w;
+}
+
+// Which slot rows a segment of expert work covers.
+//   dedup:    segment u < U is expert uniq[u], slots perm[offs[u] .. offs[u+1]);
+//             segment U (if a shared expert exists) is the shared expert on
+//             slots n*k + t for every token t.
+//   per-slot: segment s < n*k is expert ids[s] on slot s alone; segment
+//             n*k + t is the shared expert on slot n*k + t alone.
+struct SegTables {
+  const int32_t *ids;     // [n*k]
+  const int32_t *uniq;    // dedup only
+  const int32_t *offs;    // dedup only
+  const int32_t *perm;    // dedup only
+  const int32_t *n_uniq;  // dedup only
+  int32_t n, k, n_experts, n_shared;
+  int32_t dedup;  // 1 = deduplicating engine, 0 = per-slot
+};
+
+struct Seg {
+  int32_t expert;  // -1 = shared expert, -2 = invalid id (skip)
+  int32_t m;       // tokens (slots) in the segment
+  int32_t first;   // dedup: offset into perm; per-slot: the slot index
+};
+
+__device__ __forceinline__ int32_t n_segments(const SegTables &T) {
+  if (T.dedup) return __ldg(T.n_uniq) + T.n_shared;
+  return T.n * T.k + T.n_shared * T.n;
+}
+
+__device__ __forceinline__ Seg get_segment(const SegTables &T, int32_t u) {
+  Seg s;
+  const int32_t nk = T.n * T.k;
+  if (T.dedup) {
+    const int32_t U = __ldg(T.n_uniq);
+    if (u < U) {
+      s.expert = __ldg(T.uniq + u);
+      s.first = __ldg(T.offs + u);
+      s.m = __ldg(T.offs + u + 1) - s.first;
+    } else {
+      s.expert = -1;
+      s.first = 0;
+      s.m = T.n;
+    }
+  } else {
+    s.m = 1;
+    s.first = u;
+    if (u < nk) {
+      const int32_t e = __ldg(T.ids + u);
+      s.expert = (e >= 0 && e < T.n_experts) ? e : -2;
+    } else {
+      s.expert = -1;
+    }
+  }
+  return s;
+}
+
+// Slot index of the i-th token of segment s.
+__device__ __forceinline__ int32_t segment_slot(const SegTables &T, const Seg &s, int32_t i) {
+  if (!T.dedup) return s.first;
+  if (s.expert == -1) return T.n * T.k + i;
+  return __ldg(T.perm + s.first + i);
+}
+
+__device__ __forceinline__ int32_t slot_token(const SegTables &T, int32_t slot) {
+  const int32_t nk = T.n * T.k;
+  return slot < nk ? slot / T.k : slot - nk;
+}
+
+}  // namespace moe

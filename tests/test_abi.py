@@ -1,0 +1,117 @@
+"""The C-ABI library loads and exports every symbol include/moe_verify.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from moe_expert_ffn_gemv_gb300 import build
+    build.build()
+    from moe_expert_ffn_gemv_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls_of_the_path():
+    names = declared_functions()
+    for f in ("moe_route_topk", "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(cdll, name), name
+    assert sorted(lib.EXPORTED) == declared_functions()
+
+
+def test_library_exports_nothing_else(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    ours = sorted(l.split()[-1] for l in out.splitlines() if " T " in l and "moe_" in l)
+    assert ours == declared_functions()
+
+
+def _desc(lib, **kw):
+    base = dict(d=7168, n_experts=256, top_k=8, inter=2048, n_shared=1, n_max=64,
+                act_dtype=lib.MOE_BF16, w_dtype=lib.MOE_E4M3_B128,
+                gate=lib.MOE_GATE_SIGMOID_RENORM, wait_timeout_us=0)
+    base.update(kw)
+    return lib.moe_layer_desc(**base)
+
+
+def test_expert_bytes_through_the_abi(lib):
+    # one DeepSeek-V3 FP8 expert: 44,040,192 weight bytes + 10,752 scale bytes
+    assert lib.moe_expert_bytes(_desc(lib)) == (44_040_192, 10_752)
+    # one Qwen3-30B-A3B bf16 expert: 9,437,184 bytes
+    d = _desc(lib, d=2048, n_experts=128, inter=768, n_shared=0, w_dtype=lib.MOE_BF16)
+    assert lib.moe_expert_bytes(d) == (9_437_184, 0)
+
+
+def test_workspace_bytes_and_desc_checks(lib):
+    assert lib.moe_workspace_bytes(_desc(lib)) > 0
+    bad = [dict(d=0), dict(top_k=0), dict(top_k=300), dict(n_experts=-1), dict(n_shared=-1),
+           dict(act_dtype=9), dict(w_dtype=7), dict(gate=5), dict(wait_timeout_us=-3)]
+    for kw in bad:
+        assert lib.moe_workspace_bytes(_desc(lib, **kw)) == 0, kw
+    unsupported = [dict(n_experts=512, top_k=8), dict(top_k=33, n_experts=64), dict(n_max=65),
+                   dict(n_shared=2), dict(d=7200), dict(inter=2000), dict(act_dtype=lib.MOE_F32),
+                   dict(w_dtype=lib.MOE_BF16, d=2080)]
+    for kw in unsupported:
+        with pytest.raises(lib.MoeError) as e:
+            lib.moe_expert_bytes(_desc(lib, **kw))
+        assert e.value.status == lib.MOE_ERR_UNSUPPORTED, kw
+
+
+def test_launching_calls_reject_bad_arguments_before_any_launch(lib):
+    D = _desc(lib)
+    P = ctypes.c_void_p
+    r = lib._lib
+    s0 = P(0)
+    assert r.moe_route_topk(ctypes.byref(D), None, None, 4, None, None, None, s0) == lib.MOE_ERR_INVALID_ARG
+    # misaligned pointers
+    x = P(0x1008)
+    assert r.moe_route_topk(ctypes.byref(D), x, x, 4, x, x, x, s0) == lib.MOE_ERR_ALIGNMENT
+    # n beyond n_max
+    y = P(0x1000)
+    assert r.moe_route_topk(ctypes.byref(D), y, y, 65, y, y, y, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_topk_from_logits(ctypes.byref(D), y, -1, y, y, s0) == lib.MOE_ERR_INVALID_ARG
+    W = lib.moe_expert_weights(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    plan = lib.moe_plan(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    nb = lib.moe_workspace_bytes(D)
+    # workspace too small
+    assert r.moe_verify_dedup(ctypes.byref(D), ctypes.byref(W), y, 8, y, y, ctypes.byref(plan), y,
+                              nb - 1, y, s0) == lib.MOE_ERR_WORKSPACE
+    # missing scales for E4M3 weights
+    W2 = lib.moe_expert_weights(0x1000, 0x1000, None, None, 0x1000, 0x1000, 0x1000, 0x1000)
+    assert r.moe_verify_perslot(ctypes.byref(D), ctypes.byref(W2), y, 8, y, y, y, nb, y,
+                                s0) == lib.MOE_ERR_INVALID_ARG
+    # missing shared expert when the desc has one
+    W3 = lib.moe_expert_weights(0x1000, 0x1000, 0x1000, 0x1000, None, None, None, None)
+    assert r.moe_verify_perslot(ctypes.byref(D), ctypes.byref(W3), y, 8, y, y, y, nb, y,
+                                s0) == lib.MOE_ERR_INVALID_ARG
+    # plan without arrays
+    empty_plan = lib.moe_plan(None, None, None, None, None, None)
+    assert r.moe_union_plan(ctypes.byref(D), y, 8, ctypes.byref(empty_plan), None,
+                            s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_selftest_bounded_wait(y, 0, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_last_error(None, s0) == lib.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.moe_status_string(s) not in ("", "unknown status")
+    assert lib.moe_status_string(99) == "unknown status"

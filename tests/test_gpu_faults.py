@@ -1,0 +1,75 @@
+"""Failure handling on the GPU, without faulting it: bounded waits that run
+out return an error status and leave the context usable; device-side bad
+ids are reported, not followed."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_ffn_gemv_gb300 import synth
+from tests.helpers import TOL, np_bytes, oracle_layer, rel_err
+
+pytestmark = pytest.mark.gpu
+
+SMALL = synth.LayerConfig("fp8-fault", 256, 8, 2, 128, synth.BF16, synth.E4M3,
+                          synth.GATE_SIGMOID_RENORM, n_shared=1)
+
+
+@pytest.fixture(scope="module")
+def mv():
+    from moe_expert_ffn_gemv_gb300 import binding
+    return binding
+
+
+def test_bounded_wait_runs_out_and_reports(mv):
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    mv.moe_selftest_bounded_wait(err, 2000)   # a barrier nothing arrives on; 2 ms limit
+    torch.cuda.synchronize()
+    assert int(err[0]) == mv.MOE_ERR_TIMEOUT
+    # the context is still usable
+    x = torch.arange(10, device="cuda").sum().item()
+    assert x == 45
+
+
+def _pass(mv, layer, h, n, timeout_us):
+    vl = mv.VerifyLayer(layer, n, wait_timeout_us=timeout_us)
+    vl.route(h, n)
+    vl.union_plan(n)
+    y = vl.dedup(h, n).float().cpu().numpy()
+    return y, vl.last_error()
+
+
+def test_tiny_wait_limit_ends_cleanly_then_normal_call_is_right(mv):
+    layer = synth.make_layer(SMALL, seed=4).to("cuda")
+    h = synth.make_hidden(SMALL, 8, seed=5)
+    hd = h.cuda()
+    # a 1 microsecond limit: waits may run out; the call must end with OK or
+    # TIMEOUT, never hang
+    for _ in range(3):
+        _, status = _pass(mv, layer, hd, 8, 1)
+        assert status in (mv.MOE_OK, mv.MOE_ERR_TIMEOUT)
+    y, status = _pass(mv, layer, hd, 8, 0)
+    assert status == mv.MOE_OK
+    L = oracle_layer(layer.to("cpu"))
+    _, _, _, y_ref = oracle.verify(L, np_bytes(h))
+    assert rel_err(y, y_ref) <= TOL[SMALL.wtype]
+
+
+def test_out_of_range_ids_are_reported_by_both_engines(mv):
+    layer = synth.make_layer(SMALL, seed=4).to("cuda")
+    n = 4
+    h = synth.make_hidden(SMALL, n, seed=5).cuda()
+    vl = mv.VerifyLayer(layer, n)
+    ids = np.array([[0, 1], [2, 99], [3, -5], [4, 5]], dtype=np.int32)
+    vl.ids[:8].copy_(torch.from_numpy(ids.ravel()))
+    vl.w[:8].fill_(0.5)
+    vl.perslot(h, n)
+    assert vl.last_error() == mv.MOE_ERR_DEVICE_INPUT
+    vl.union_plan(n)
+    vl.dedup(h, n)
+    assert vl.last_error() == mv.MOE_ERR_DEVICE_INPUT
+    # a clean call afterwards reports OK
+    vl.route(h, n)
+    vl.union_plan(n)
+    vl.dedup(h, n)
+    assert vl.last_error() == mv.MOE_OK
