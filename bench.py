@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-sweep", action="store_true", help="skip the n = 1..64 engine sweep")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     p.add_argument("--sweep-max", type=int, default=64)
+    p.add_argument("--experts", type=int, default=None,
+                   help="routed experts of the layer (default 256); fewer make a small profiling case")
     return p.parse_args()
 
 
@@ -183,6 +185,8 @@ def csrc_hash() -> str:
 
 def make_workload(device="cuda"):
     layer = synth.make_layer(CFG, seed=1, device=device)
+    if layer.cfg.n_experts != CFG.n_experts:
+        raise AssertionError("layer config mismatch")
     h = synth.make_hidden(CFG, 64, seed=3, device=device)   # the first n nodes of a 64-node tree
     return layer, h
 
@@ -448,7 +452,12 @@ def run_reference(args):
 
 
 def main():
+    global CFG, WORKLOAD
     args = parse()
+    if args.experts:
+        from dataclasses import replace
+        CFG = replace(CFG, n_experts=args.experts)
+        WORKLOAD += f" ({args.experts} routed experts: profiling case)"
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -30,7 +30,9 @@
  *     the host, so a whole pass can be captured in a CUDA graph.  The one
  *     exception is moe_last_error(), which synchronises `stream`.
  *   - Arguments are checked on the host before anything is enqueued; a bad
- *     argument returns a non-OK status and enqueues nothing.
+ *     argument returns a non-OK status and enqueues nothing.  With n == 0 a
+ *     call reads and writes nothing, so its array pointers may be NULL
+ *     (moe_union_plan still writes U = 0 and offs[0] = 0).
  *   - Device arrays must start on a 16-byte boundary.
  *   - Outputs are fully overwritten.  No C++ exception crosses this ABI.
  *   - Layout of a layer (row-major everywhere):

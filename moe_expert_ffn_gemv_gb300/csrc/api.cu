@@ -188,6 +188,7 @@ moe_status check_verify_args(const moe_layer_desc *desc, const moe_expert_weight
   moe_status s = check_desc(desc);
   if (s != MOE_OK) return s;
   if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;  // nothing is read or written
   s = check_weights(*desc, weights);
   if (s != MOE_OK) return s;
   if (!h || !ids || !w || !workspace || !y) return MOE_ERR_INVALID_ARG;
@@ -245,11 +246,11 @@ MOE_API moe_status moe_route_topk(const moe_layer_desc *desc, const void *router
   moe_status s = check_desc(desc);
   if (s != MOE_OK) return s;
   if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;  // nothing is read or written
   if (!router_w || !h || !ids || !w || !logits) return MOE_ERR_INVALID_ARG;
   if (!aligned16(router_w) || !aligned16(h) || !aligned16(ids) || !aligned16(w) ||
       !aligned16(logits))
     return MOE_ERR_ALIGNMENT;
-  if (n == 0) return MOE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_router_scores(desc->act_dtype == MOE_BF16, router_w, h, n, desc->d,
                                        desc->n_experts, logits, st);
@@ -263,9 +264,9 @@ MOE_API moe_status moe_topk_from_logits(const moe_layer_desc *desc, const float 
   moe_status s = check_desc(desc);
   if (s != MOE_OK) return s;
   if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;  // nothing is read or written
   if (!logits || !ids || !w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(ids) || !aligned16(w)) return MOE_ERR_ALIGNMENT;
-  if (n == 0) return MOE_OK;
   return cuda_status(launch_topk_gate(logits, n, desc->n_experts, desc->top_k, desc->gate, ids, w,
                                       static_cast<cudaStream_t>(stream)));
 }
