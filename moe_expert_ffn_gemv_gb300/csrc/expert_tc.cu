@@ -69,30 +69,132 @@ __device__ __forceinline__ float silu_times(float g, float u) {
   return g / (1.0f + __expf(-g)) * u;
 }
 
+// The plan (or, per-slot, the routed ids) copied to shared memory at kernel
+// start, so that stepping from one work item to the next costs no global
+// round trip.
+constexpr int MAX_SLOTS = 64 * 32;
+constexpr int MAX_EXPERTS = 256;
+
+struct LocalTables {
+  const int32_t *uniq;  // [U]      dedup
+  const int32_t *offs;  // [U + 1]  dedup
+  const int32_t *tab;   // [n*k]    dedup: perm; per-slot: ids
+  int U, n, k, n_experts, n_shared, dedup;
+
+  __device__ int n_segments() const { return dedup ? U + n_shared : n * k + n_shared * n; }
+
+  __device__ Seg segment(int u) const {
+    Seg s;
+    const int nk = n * k;
+    if (dedup) {
+      if (u < U) {
+        s.expert = uniq[u];
+        s.first = offs[u];
+        s.m = offs[u + 1] - s.first;
+      } else {
+        s.expert = -1;
+        s.first = 0;
+        s.m = n;
+      }
+    } else {
+      s.m = 1;
+      s.first = u;
+      if (u < nk) {
+        const int e = tab[u];
+        s.expert = (e >= 0 && e < n_experts) ? e : -2;
+      } else {
+        s.expert = -1;
+      }
+    }
+    return s;
+  }
+  // slot index of the i-th token of segment s
+  __device__ int slot(const Seg &s, int i) const {
+    if (!dedup) return s.first;
+    if (s.expert == -1) return n * k + i;
+    return tab[s.first + i];
+  }
+  __device__ int token(int slot) const { return slot < n * k ? slot / k : slot - n * k; }
+};
+
+// Position in the (item, token group, K stage) sequence a CTA walks.  The
+// producer and all consumer warps walk the same sequence.
+struct Cursor {
+  int item, rb, grp, ks, groups;
+  Seg sg;
+};
+
+template <int TOK>
+__device__ __forceinline__ bool cursor_item(Cursor &c, const LocalTables &T, int n_items,
+                                            int row_blocks, int32_t *err, bool report) {
+  while (c.item < n_items) {
+    const int u = c.item / row_blocks;
+    c.rb = c.item - u * row_blocks;
+    c.sg = T.segment(u);
+    if (c.sg.expert != -2) {
+      c.groups = (c.sg.m + TOK - 1) / TOK;
+      c.grp = 0;
+      c.ks = 0;
+      return true;
+    }
+    if (report && c.rb == 0) record_error(err, MOE_ERR_DEVICE_INPUT);
+    c.item += gridDim.x;
+  }
+  return false;
+}
+
+template <int TOK>
+__device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int n_items,
+                                            int row_blocks, int kstages, int32_t *err,
+                                            bool report) {
+  if (++c.ks < kstages) return true;
+  c.ks = 0;
+  if (++c.grp < c.groups) return true;
+  c.item += gridDim.x;
+  return cursor_item<TOK>(c, T, n_items, row_blocks, err, report);
+}
+
 template <bool FP8, int PHASE, int NT>
 __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P) {
   constexpr int S = n_stages<NT>();
   constexpr int ES = FP8 ? 1 : 2;       // bytes per weight element
   constexpr int TOK = 8 * NT;           // tokens per pass over an item
+  constexpr int BW = FP8 ? 8 : 4;       // B-fragment words per N tile and stage
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
   float4 *red = reinterpret_cast<float4 *>(smem + S * STAGE_BYTES);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * STAGE_BYTES + red_bytes<NT>());
   uint64_t *empty = full + S;
   __shared__ volatile int s_abort;
+  __shared__ int32_t s_uniq[MAX_EXPERTS];
+  __shared__ int32_t s_offs[MAX_EXPERTS + 1];
+  __shared__ int32_t s_tab[MAX_SLOTS];
+  __shared__ int32_t s_U;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = P.T.n * P.T.k;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], CONSUMERS);
     }
     s_abort = 0;
+    s_U = P.T.dedup ? *P.T.n_uniq : 0;
     fence_barrier_init();
   }
+  {
+    const int32_t *src = P.T.dedup ? P.T.perm : P.T.ids;
+    for (int i = threadIdx.x; i < nk; i += THREADS) s_tab[i] = src[i];
+    if (P.T.dedup)
+      for (int i = threadIdx.x; i <= P.T.n_experts; i += THREADS) {
+        if (i < P.T.n_experts) s_uniq[i] = P.T.uniq[i];
+        s_offs[i] = P.T.offs[i];
+      }
+  }
   __syncthreads();
+  LocalTables T{s_uniq, s_offs, s_tab, s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared, P.T.dedup};
 
-  const int n_items = n_segments(P.T) * P.row_blocks;
+  const int n_items = T.n_segments() * P.row_blocks;
   const int kbytes = P.kdim * ES;
   const int kstages = (kbytes + KBYTES - 1) / KBYTES;
   const int scale_cols = P.kdim / 128;              // E4M3 scale table width
@@ -103,34 +205,32 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     const uint64_t policy = policy_evict_first();
     uint32_t it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int u = item / P.row_blocks, rb = item - u * P.row_blocks;
-      const Seg sg = get_segment(P.T, u);
-      if (sg.expert == -2) continue;
-      const int groups = (sg.m + TOK - 1) / TOK;
-      const uint8_t *base = sg.expert >= 0 ? P.w + int64_t(sg.expert) * P.expert_stride : P.w_sh;
-      for (int grp = 0; grp < groups && ok; ++grp) {
-        for (int ks = 0; ks < kstages; ++ks, ++it) {
-          const int s = it % S;
-          const uint32_t round = it / S;
-          if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1, P.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          if (s_abort) { ok = false; break; }
-          const int k0 = ks * KBYTES;
-          const int nb = min(KBYTES, kbytes - k0);
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(ROWS * nb));
-          __syncwarp();
-          for (int r = lane; r < ROWS; r += 32) {
-            int grow;
-            if (PHASE == 1) grow = r < 32 ? rb * 32 + r : P.inter + rb * 32 + (r - 32);
-            else grow = rb * ROWS + r;
-            bulk_g2s(ring + s * STAGE_BYTES + r * ROW_STRIDE, base + int64_t(grow) * kbytes + k0,
-                     uint32_t(nb), &full[s], policy);
-          }
-        }
+    Cursor cur;
+    cur.item = blockIdx.x;
+    bool have = cursor_item<TOK>(cur, T, n_items, P.row_blocks, P.err, false);
+    while (have) {
+      const int s = it % S;
+      const uint32_t round = it / S;
+      if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1, P.timeout_ns)) {
+        ok = false;
+        break;
       }
+      if (s_abort) { ok = false; break; }
+      const uint8_t *base =
+          cur.sg.expert >= 0 ? P.w + int64_t(cur.sg.expert) * P.expert_stride : P.w_sh;
+      const int k0 = cur.ks * KBYTES;
+      const int nb = min(KBYTES, kbytes - k0);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(ROWS * nb));
+      __syncwarp();
+      for (int r = lane; r < ROWS; r += 32) {
+        int grow;
+        if (PHASE == 1) grow = r < 32 ? cur.rb * 32 + r : P.inter + cur.rb * 32 + (r - 32);
+        else grow = cur.rb * ROWS + r;
+        bulk_g2s(ring + s * STAGE_BYTES + r * ROW_STRIDE, base + int64_t(grow) * kbytes + k0,
+                 uint32_t(nb), &full[s], policy);
+      }
+      ++it;
+      have = cursor_next<TOK>(cur, T, n_items, P.row_blocks, kstages, P.err, false);
     }
     if (!ok) {
       if (lane == 0) {
@@ -156,126 +256,148 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   uint32_t it = 0;
   bool aborted = false;
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int u = item / P.row_blocks, rb = item - u * P.row_blocks;
-    const Seg sg = get_segment(P.T, u);
-    if (sg.expert == -2) {
-      if (tid == 0 && rb == 0) record_error(P.err, MOE_ERR_DEVICE_INPUT);
-      continue;
+  // activation row of this lane's token in each N tile (-1: none)
+  auto rows_of = [&](const Cursor &q, int (&arow)[NT]) {
+    const int m_left = q.sg.m - q.grp * TOK;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = nt * 8 + g;
+      arow[nt] = -1;
+      if (col < m_left) {
+        const int slot = T.slot(q.sg, q.grp * TOK + col);
+        arow[nt] = PHASE == 1 ? T.token(slot) : slot;
+      }
     }
-    const int groups = (sg.m + TOK - 1) / TOK;
-    const float *scales = nullptr;
-    if (FP8) scales = sg.expert >= 0 ? P.sc + int64_t(sg.expert) * scale_stride : P.sc_sh;
-    // E4M3 scale rows of the two halves of the stage (phase 1: gate, up)
-    const int srow_a = PHASE == 1 ? (rb * 32) / 128 : (rb * ROWS) / 128;
-    const int srow_b = PHASE == 1 ? (P.inter + rb * 32) / 128 : srow_a;
-
-    for (int grp = 0; grp < groups; ++grp) {
-      const int m_left = sg.m - grp * TOK;   // tokens of this pass (may exceed TOK)
-      // activation row of this lane's token in each N tile
-      int arow[NT];
+  };
+  // B fragments (this lane's token, the warp's columns of stage q, in the
+  // order of the thread's weight bytes) and the stage's block scales
+  auto load_inputs = [&](const Cursor &q, const int (&arow)[NT], uint32_t (&bfr)[NT][BW],
+                         float &sc_a, float &sc_b) {
+    const int kb0 = q.ks * KBYTES + warp * 64;
+    const bool active = kb0 < kbytes;
+    const int kcol0 = kb0 / ES;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int col = nt * 8 + g;
-        arow[nt] = -1;
-        if (col < m_left) {
-          const int slot = segment_slot(P.T, sg, grp * TOK + col);
-          arow[nt] = PHASE == 1 ? slot_token(P.T, slot) : slot;
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int v = 0; v < BW; ++v) bfr[nt][v] = 0u;
+      if (active && arow[nt] >= 0) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            act + int64_t(arow[nt]) * P.kdim + kcol0 + (FP8 ? 16 * c : 8 * c));
+#pragma unroll
+        for (int v = 0; v < BW / 4; ++v) {
+          const uint4 x = __ldg(src + v);
+          bfr[nt][4 * v + 0] = x.x;
+          bfr[nt][4 * v + 1] = x.y;
+          bfr[nt][4 * v + 2] = x.z;
+          bfr[nt][4 * v + 3] = x.w;
         }
       }
-      float acc[4][NT][4];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
+    }
+    sc_a = sc_b = 1.f;
+    if (FP8 && active) {
+      const float *scales =
+          q.sg.expert >= 0 ? P.sc + int64_t(q.sg.expert) * scale_stride : P.sc_sh;
+      const int srow_a = PHASE == 1 ? (q.rb * 32) / 128 : (q.rb * ROWS) / 128;
+      const int srow_b = PHASE == 1 ? (P.inter + q.rb * 32) / 128 : srow_a;
+      sc_a = __ldg(scales + int64_t(srow_a) * scale_cols + kcol0 / 128);
+      sc_b = __ldg(scales + int64_t(srow_b) * scale_cols + kcol0 / 128);
+    }
+  };
 
-      for (int ks = 0; ks < kstages; ++ks, ++it) {
-        const int s = it % S;
-        const uint32_t round = it / S;
-        const int kb0 = ks * KBYTES + warp * 64;          // first byte of this warp's chunk
-        const bool active = kb0 < kbytes;
-        const int kcol0 = kb0 / ES;                        // first weight column of the chunk
-        // B fragments: this lane's token, the chunk's columns in the same order
-        // as the thread's weight bytes.
-        constexpr int BW = FP8 ? 8 : 4;
-        uint32_t bfr[NT][BW];
+  float acc[4][NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+  for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-          for (int q = 0; q < BW; ++q) bfr[nt][q] = 0u;
-          if (active && arow[nt] >= 0) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                act + int64_t(arow[nt]) * P.kdim + kcol0 + (FP8 ? 16 * c : 8 * c));
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int v = 0; v < BW / 4; ++v) {
-              const uint4 x = __ldg(src + v);
-              bfr[nt][4 * v + 0] = x.x;
-              bfr[nt][4 * v + 1] = x.y;
-              bfr[nt][4 * v + 2] = x.z;
-              bfr[nt][4 * v + 3] = x.w;
-            }
-          }
-        }
-        if (!aborted && s_abort) aborted = true;
-        if (!aborted && !mbar_wait_bounded(&full[s], round & 1, P.timeout_ns)) {
-          aborted = true;
-          s_abort = 1;
-          if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
-        }
-        if (!aborted && active) {
-          const uint8_t *st = ring + s * STAGE_BYTES + warp * 64 + c * 16;
-          float sc_a = 1.f, sc_b = 1.f;
-          if (FP8) {
-            sc_a = __ldg(scales + int64_t(srow_a) * scale_cols + kcol0 / 128);
-            sc_b = __ldg(scales + int64_t(srow_b) * scale_cols + kcol0 / 128);
-          }
+      for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
+
+  Cursor cur;
+  cur.item = blockIdx.x;
+  bool have = cursor_item<TOK>(cur, T, n_items, P.row_blocks, P.err, tid == 0);
+  int arow[NT];
+  uint32_t bfr[NT][BW];
+  float sc_a = 1.f, sc_b = 1.f;
+  if (have) {
+    rows_of(cur, arow);
+    load_inputs(cur, arow, bfr, sc_a, sc_b);
+  }
+
+  while (have) {
+    // prefetch the next stage's activations and scales
+    Cursor nxt = cur;
+    const bool have_next = cursor_next<TOK>(nxt, T, n_items, P.row_blocks, kstages, P.err, tid == 0);
+    int arow_n[NT];
+    uint32_t bfr_n[NT][BW];
+    float sc_an = 1.f, sc_bn = 1.f;
+    if (have_next) {
+      if (nxt.ks == 0) rows_of(nxt, arow_n);
+      else {
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint4 lo = *reinterpret_cast<const uint4 *>(st + (mt * 16 + g) * ROW_STRIDE);
-            const uint4 hi = *reinterpret_cast<const uint4 *>(st + (mt * 16 + g + 8) * ROW_STRIDE);
-            const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
-            const uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
-            if (FP8) {
-              float tmp[NT][4];
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tmp[nt][q] = 0.f;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(wl[j]);
-                a[1] = e4m3x2_to_f16x2(wh[j]);
-                a[2] = e4m3x2_to_f16x2(wl[j] >> 16);
-                a[3] = e4m3x2_to_f16x2(wh[j] >> 16);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                  if (nt * 8 < m_left) mma_16816<false>(tmp[nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);
-              }
-              const float scl = mt < 2 ? sc_a : sc_b;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[mt][nt][q] = fmaf(scl, tmp[nt][q], acc[mt][nt][q]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const uint32_t a[4] = {wl[2 * j], wh[2 * j], wl[2 * j + 1], wh[2 * j + 1]};
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                  if (nt * 8 < m_left)
-                    mma_16816<true>(acc[mt][nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);
-              }
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        for (int nt = 0; nt < NT; ++nt) arow_n[nt] = arow[nt];
       }
+      load_inputs(nxt, arow_n, bfr_n, sc_an, sc_bn);
+    }
 
-      // ---- epilogue: add the 8 warps' K-partials in a fixed order
+    const int s = it % S;
+    const uint32_t round = it / S;
+    const int m_left = cur.sg.m - cur.grp * TOK;
+    const bool active = cur.ks * KBYTES + warp * 64 < kbytes;
+    if (!aborted && s_abort) aborted = true;
+    if (!aborted && !mbar_wait_bounded(&full[s], round & 1, P.timeout_ns)) {
+      aborted = true;
+      s_abort = 1;
+      if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+    }
+    if (!aborted && active) {
+      const uint8_t *st = ring + s * STAGE_BYTES + warp * 64 + c * 16;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const uint4 lo = *reinterpret_cast<const uint4 *>(st + (mt * 16 + g) * ROW_STRIDE);
+        const uint4 hi = *reinterpret_cast<const uint4 *>(st + (mt * 16 + g + 8) * ROW_STRIDE);
+        const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
+        const uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
+        if (FP8) {
+          float tmp[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmp[nt][q] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t a[4];
+            a[0] = e4m3x2_to_f16x2(wl[j]);
+            a[1] = e4m3x2_to_f16x2(wh[j]);
+            a[2] = e4m3x2_to_f16x2(wl[j] >> 16);
+            a[3] = e4m3x2_to_f16x2(wh[j] >> 16);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt * 8 < m_left) mma_16816<false>(tmp[nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);
+          }
+          const float scl = mt < 2 ? sc_a : sc_b;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mt][nt][q] = fmaf(scl, tmp[nt][q], acc[mt][nt][q]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t a[4] = {wl[2 * j], wh[2 * j], wl[2 * j + 1], wh[2 * j + 1]};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              if (nt * 8 < m_left)
+                mma_16816<true>(acc[mt][nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    ++it;
+
+    if (cur.ks == kstages - 1) {
+      // ---- epilogue of (item, token group): add the 8 warps' K-partials in
+      // a fixed order, then silu(g)*u (phase 1) or the fp32 rows (phase 2)
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
@@ -304,22 +426,41 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
           for (int e = 0; e < 4; ++e) {
             const int row = mt * 16 + gg + (e >> 1) * 8;
             const int col = nt * 8 + 2 * cc + (e & 1);
-            if (col >= m_left || col >= TOK) continue;
-            const int slot = segment_slot(P.T, sg, grp * TOK + col);
+            if (col >= m_left) continue;
+            const int slot = T.slot(cur.sg, cur.grp * TOK + col);
             if (PHASE == 1) {
               const float a = silu_times(vals[e], ups[e]);
-              uint16_t *out = static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter + rb * 32 + row;
+              uint16_t *out =
+                  static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter + cur.rb * 32 + row;
               if (FP8) *reinterpret_cast<__half *>(out) = __float2half_rn(a);
               else *reinterpret_cast<__nv_bfloat16 *>(out) = __float2bfloat16_rn(a);
             } else {
-              float *out = static_cast<float *>(P.out) + int64_t(slot) * P.rows_total + rb * ROWS + row;
+              float *out = static_cast<float *>(P.out) + int64_t(slot) * P.rows_total +
+                           cur.rb * ROWS + row;
               *out = vals[e];
             }
           }
         }
       }
       consumer_sync();
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
     }
+
+    cur = nxt;
+    have = have_next;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      arow[nt] = arow_n[nt];
+#pragma unroll
+      for (int v = 0; v < BW; ++v) bfr[nt][v] = bfr_n[nt][v];
+    }
+    sc_a = sc_an;
+    sc_b = sc_bn;
   }
 }
 
