@@ -46,6 +46,10 @@
  *       y          [n][d]           act_dtype
  *     An E4M3 weight is q * s where q is the OCP FP8 E4M3 value of the byte
  *     and s the fp32 scale of its 128 x 128 block.
+ *   - Packed weights: moe_verify_dedup and moe_verify_perslot read w13, w2,
+ *     sh_w13 and sh_w2 in the tile layout that moe_pack_expert_weights
+ *     writes once, when the model is loaded (same size as the row-major
+ *     arrays; identical to them for F32).  Scales stay row-major.
  *   - Limits (else MOE_ERR_UNSUPPORTED): N <= 256, 1 <= k <= min(N, 32),
  *     0 <= n <= n_max <= 64, n_shared 0 or 1, d % 8 == 0; F32 weights go with
  *     F32 activations and need I % 4 == 0; BF16 and E4M3 weights go with BF16
@@ -102,8 +106,8 @@ typedef struct {
 } moe_layer_desc;
 
 typedef struct {
-  const void *w13;    /* device, [N][2I][d]                         */
-  const void *w2;     /* device, [N][d][I]                          */
+  const void *w13;    /* device, [N][2I][d], packed                 */
+  const void *w2;     /* device, [N][d][I], packed                  */
   const float *s13;   /* device, E4M3 only, else NULL               */
   const float *s2;    /* device, E4M3 only, else NULL               */
   const void *sh_w13; /* device, shared expert [2I][d]; NULL if none */
@@ -136,6 +140,21 @@ size_t moe_workspace_bytes(const moe_layer_desc *desc);
  * pointer may be NULL. */
 moe_status moe_expert_bytes(const moe_layer_desc *desc, int64_t *weight_bytes,
                             int64_t *scale_bytes);
+
+/* Repacks n_matrices experts' W13 and W2 (device, row-major as in the layout
+ * above) into the tile layout the expert engines stream (device, caller
+ * allocated, same sizes, not in place).  BF16 and E4M3: each expert matrix
+ * becomes a sequence of tiles of 64 rows x 512 bytes (the last tile of a row
+ * block narrower when a row is not a multiple of 512 bytes); a W13 tile
+ * holds gate rows 32b..32b+31 followed by up rows I+32b..I+32b+31; inside a
+ * tile the 16-byte pieces are ordered [64-byte column chunk][16-row tile]
+ * [row half][lane] so that one pipeline stage is one contiguous bulk copy.
+ * F32: a plain copy.  Call once per layer (N routed experts) and once for
+ * the shared expert (n_matrices = 1). */
+moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const void *w13,
+                                   const void *w2, int32_t n_matrices,
+                                   void *w13_packed, void *w2_packed,
+                                   moe_stream_t stream);
 
 /* Router scores and top-k ("Making Every Verified Token Count", Sec. 2.2,
  * eq. (4)).  For each of the n tokens: logits[t][e] = sum_i router_w[e][i] *

@@ -33,7 +33,8 @@ MOE_GATE_SOFTMAX, MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1, 2
 
 EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_topk_from_logits",
             "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot", "moe_workspace_init",
-            "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string"]
+            "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
+            "moe_pack_expert_weights"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -70,6 +71,8 @@ _lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ct
 _lib.moe_verify_perslot.restype = ctypes.c_int
 _lib.moe_verify_perslot.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32,
                                     _P, _P, _P, ctypes.c_size_t, _P, _P]
+_lib.moe_pack_expert_weights.restype = ctypes.c_int
+_lib.moe_pack_expert_weights.argtypes = [_D, _P, _P, ctypes.c_int32, _P, _P, _P]
 _lib.moe_workspace_init.restype = ctypes.c_int
 _lib.moe_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
 _lib.moe_last_error.restype = ctypes.c_int
@@ -150,6 +153,12 @@ def moe_verify_perslot(desc, weights: moe_expert_weights, h, n, ids, w, workspac
                                    _stream(stream)), "moe_verify_perslot")
 
 
+def moe_pack_expert_weights(desc, w13, w2, n_matrices, w13_packed, w2_packed, stream=None) -> None:
+    _check(_lib.moe_pack_expert_weights(ctypes.byref(desc), _ptr(w13), _ptr(w2), n_matrices,
+                                        _ptr(w13_packed), _ptr(w2_packed), _stream(stream)),
+           "moe_pack_expert_weights")
+
+
 def moe_workspace_init(workspace, stream=None) -> None:
     _check(_lib.moe_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "moe_workspace_init")
@@ -177,10 +186,35 @@ def make_desc(cfg: synth.LayerConfig, n_max: int, wait_timeout_us: int = 0) -> m
                           _DT[cfg.act], _DT[cfg.wtype], _GATE[cfg.gate], wait_timeout_us)
 
 
-def make_weights(layer: synth.Layer) -> moe_expert_weights:
-    return moe_expert_weights(_ptr(layer.w13), _ptr(layer.w2), _ptr(layer.s13), _ptr(layer.s2),
-                              _ptr(layer.sh_w13), _ptr(layer.sh_w2), _ptr(layer.sh_s13),
-                              _ptr(layer.sh_s2))
+@dataclass
+class PackedWeights:
+    """A layer's expert weights in the library's packed tile layout (device)."""
+    w13: torch.Tensor
+    w2: torch.Tensor
+    sh_w13: Optional[torch.Tensor]
+    sh_w2: Optional[torch.Tensor]
+    s13: Optional[torch.Tensor]
+    s2: Optional[torch.Tensor]
+    sh_s13: Optional[torch.Tensor]
+    sh_s2: Optional[torch.Tensor]
+
+    def c(self) -> moe_expert_weights:
+        return moe_expert_weights(_ptr(self.w13), _ptr(self.w2), _ptr(self.s13), _ptr(self.s2),
+                                  _ptr(self.sh_w13), _ptr(self.sh_w2), _ptr(self.sh_s13),
+                                  _ptr(self.sh_s2))
+
+
+def pack_weights(layer: synth.Layer, desc: moe_layer_desc) -> PackedWeights:
+    """Repack a layer's (device, row-major) expert weights with moe_pack_expert_weights."""
+    w13 = torch.empty_like(layer.w13)
+    w2 = torch.empty_like(layer.w2)
+    moe_pack_expert_weights(desc, layer.w13, layer.w2, layer.cfg.n_experts, w13, w2)
+    sh13 = sh2 = None
+    if layer.sh_w13 is not None:
+        sh13 = torch.empty_like(layer.sh_w13)
+        sh2 = torch.empty_like(layer.sh_w2)
+        moe_pack_expert_weights(desc, layer.sh_w13, layer.sh_w2, 1, sh13, sh2)
+    return PackedWeights(w13, w2, sh13, sh2, layer.s13, layer.s2, layer.sh_s13, layer.sh_s2)
 
 
 @dataclass
@@ -205,8 +239,9 @@ def _aligned_empty(count: int, dtype, device) -> torch.Tensor:
 class VerifyLayer:
     """Device buffers of one layer and the calls of one verification pass.
 
-    Owns nothing but torch tensors; every method is one or more C calls on the
-    current stream.  `weights` must stay alive as long as this object.
+    Owns nothing but torch tensors (its packed copy of the expert weights,
+    the workspace, routing and plan buffers); every method is one or more C
+    calls on the current stream.
     """
 
     def __init__(self, layer: synth.Layer, n_max: int, device="cuda", wait_timeout_us: int = 0):
@@ -215,7 +250,8 @@ class VerifyLayer:
         self.cfg = cfg
         self.n_max = n_max
         self.desc = make_desc(cfg, n_max, wait_timeout_us)
-        self.weights = make_weights(layer)
+        self.packed = pack_weights(layer, self.desc)
+        self.weights = self.packed.c()
         nb = moe_workspace_bytes(self.desc)
         if nb == 0:
             raise MoeError(MOE_ERR_UNSUPPORTED, "moe_workspace_bytes")

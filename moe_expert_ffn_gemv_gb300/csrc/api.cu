@@ -315,6 +315,35 @@ MOE_API moe_status moe_verify_perslot(const moe_layer_desc *desc,
                      static_cast<cudaStream_t>(stream));
 }
 
+MOE_API moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const void *w13,
+                                           const void *w2, int32_t n_matrices, void *w13_packed,
+                                           void *w2_packed, moe_stream_t stream) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n_matrices < 0) return MOE_ERR_INVALID_ARG;
+  if (n_matrices == 0) return MOE_OK;
+  if (!w13 || !w2 || !w13_packed || !w2_packed) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w13) || !aligned16(w2) || !aligned16(w13_packed) || !aligned16(w2_packed))
+    return MOE_ERR_ALIGNMENT;
+  if (w13 == w13_packed || w2 == w2_packed) return MOE_ERR_INVALID_ARG;  // not in place
+  const moe_layer_desc &L = *desc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t es = w_size(L);
+  const size_t n13 = size_t(n_matrices) * 2 * L.inter * L.d * es;
+  const size_t n2 = size_t(n_matrices) * L.d * L.inter * es;
+  cudaError_t e;
+  if (L.w_dtype == MOE_F32) {
+    // the fp32 kernel reads the row-major layout itself
+    e = cudaMemcpyAsync(w13_packed, w13, n13, cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(w2_packed, w2, n2, cudaMemcpyDeviceToDevice, st);
+  } else {
+    e = launch_pack(w13, w13_packed, n_matrices, 2 * L.inter, int(L.d * es), L.inter, true, st);
+    if (e == cudaSuccess)
+      e = launch_pack(w2, w2_packed, n_matrices, L.d, int(L.inter * es), L.inter, false, st);
+  }
+  return cuda_status(e);
+}
+
 MOE_API moe_status moe_workspace_init(void *workspace, size_t ws_bytes, moe_stream_t stream) {
   if (!workspace || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return MOE_ERR_ALIGNMENT;

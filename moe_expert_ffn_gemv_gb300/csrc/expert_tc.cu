@@ -15,19 +15,26 @@
 //            writes yslot[slot][d] (fp32).
 //
 // Structure (one CTA per SM, persistent over work items (segment, row block)):
-//   - warp 8 is the producer: it streams 64 weight rows x 512 bytes per stage
-//     with 1-D TMA bulk copies (cp.async.bulk, completing on an mbarrier) into
-//     a 4- or 5-stage shared-memory ring;
+//   - the weights are stored pre-packed (pack.cu): the 64 rows x 512 bytes of
+//     one pipeline stage form one contiguous tile, its 16-byte pieces in the
+//     order the consumer threads read them;
+//   - warp 8 is the producer: it streams one tile per stage with a single 1-D
+//     TMA bulk copy (cp.async.bulk, completing on an mbarrier) into a 4- to
+//     6-stage shared-memory ring.  Copies of a few KB keep the copy engine at
+//     HBM speed; 512-byte copies (one per row) would not;
 //   - warps 0..7 consume: warp w owns bytes [64 w, 64 w + 64) of every row of a
 //     stage, i.e. a K-split across warps, and runs mma.sync m16n8k16 with the
 //     weights as the 16-row A operand (4 row tiles) and the segment's tokens as
 //     the 8-wide N operand (NT tiles).  Because a dot product does not depend
 //     on the order of its terms, each thread's 16 contiguous weight bytes feed
 //     the A fragment directly (no ldmatrix); the activations (B fragment) are
-//     read with the same permutation of K;
+//     read with the same permutation of K.  Each warp reads its 4 KB of a
+//     stage with lane-contiguous 16-byte loads (no bank conflicts);
 //   - E4M3 bytes become fp16 with cvt.rn.f16x2.e4m3x2 (exact); the block scale
 //     multiplies the fp32 partial sum of each 64-column chunk, which lies in a
 //     single 128x128 scale block;
+//   - the activation fragments and scales of the next stage are loaded while
+//     the current stage computes; the plan sits in shared memory;
 //   - after the last stage of an item the 8 warps' partial sums are added in
 //     shared memory in a fixed order (deterministic), and the epilogue applies
 //     silu(g)*u (phase 1) or stores the fp32 rows (phase 2).
@@ -41,17 +48,15 @@ namespace moe {
 
 namespace {
 
-constexpr int ROWS = 64;          // weight rows per stage (4 MMA row tiles)
-constexpr int KBYTES = 512;       // bytes of each row per stage
-constexpr int ROW_STRIDE = 576;   // shared-memory stride of a row: the two rows a
-                                  // quarter-warp reads sit 16 banks apart
-constexpr int STAGE_BYTES = ROWS * ROW_STRIDE;
+constexpr int ROWS = PACK_ROWS;      // weight rows per stage (4 MMA row tiles)
+constexpr int KBYTES = PACK_KBYTES;  // bytes of each row per stage
+constexpr int STAGE_BYTES = ROWS * KBYTES;
 constexpr int CONSUMERS = 8;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr uint64_t DRAIN_LIMIT_NS = 200ull * 1000 * 1000;
 
 template <int NT>
-constexpr int n_stages() { return NT >= 4 ? 4 : 5; }
+constexpr int n_stages() { return NT >= 4 ? 4 : NT == 2 ? 5 : 6; }
 
 template <int NT>
 constexpr size_t red_bytes() { return size_t(CONSUMERS) * 4 * NT * 32 * 16; }
@@ -220,15 +225,14 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
           cur.sg.expert >= 0 ? P.w + int64_t(cur.sg.expert) * P.expert_stride : P.w_sh;
       const int k0 = cur.ks * KBYTES;
       const int nb = min(KBYTES, kbytes - k0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(ROWS * nb));
-      __syncwarp();
-      for (int r = lane; r < ROWS; r += 32) {
-        int grow;
-        if (PHASE == 1) grow = r < 32 ? cur.rb * 32 + r : P.inter + cur.rb * 32 + (r - 32);
-        else grow = cur.rb * ROWS + r;
-        bulk_g2s(ring + s * STAGE_BYTES + r * ROW_STRIDE, base + int64_t(grow) * kbytes + k0,
-                 uint32_t(nb), &full[s], policy);
+      // the packed tile of (row block, K chunk): contiguous, ROWS * nb bytes
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], uint32_t(ROWS * nb));
+        bulk_g2s(ring + s * STAGE_BYTES,
+                 base + int64_t(cur.rb) * ROWS * kbytes + int64_t(k0) * ROWS,
+                 uint32_t(ROWS * nb), &full[s], policy);
       }
+      __syncwarp();
       ++it;
       have = cursor_next<TOK>(cur, T, n_items, P.row_blocks, kstages, P.err, false);
     }
@@ -350,11 +354,12 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
     }
     if (!aborted && active) {
-      const uint8_t *st = ring + s * STAGE_BYTES + warp * 64 + c * 16;
+      // this warp's 4 KB of the stage: [row tile mt][half h][lane][16 bytes]
+      const uint4 *st = reinterpret_cast<const uint4 *>(ring + s * STAGE_BYTES) + warp * 256 + lane;
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
-        const uint4 lo = *reinterpret_cast<const uint4 *>(st + (mt * 16 + g) * ROW_STRIDE);
-        const uint4 hi = *reinterpret_cast<const uint4 *>(st + (mt * 16 + g + 8) * ROW_STRIDE);
+        const uint4 lo = st[(mt * 2 + 0) * 32];
+        const uint4 hi = st[(mt * 2 + 1) * 32];
         const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
         const uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
         if (FP8) {

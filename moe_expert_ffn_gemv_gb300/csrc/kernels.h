@@ -44,6 +44,12 @@ struct F32Params {
 };
 cudaError_t launch_expert_f32(int phase, const F32Params &P, int grid, cudaStream_t stream);
 
+// Repacks n_matrices expert matrices (rows x kbytes, row-major) into the
+// tile layout of the tensor-core kernel (pack.cu); gate_up selects the W13
+// row order (gate rows, then the matching up rows, per tile).
+cudaError_t launch_pack(const void *src, void *dst, int n_matrices, int rows, int kbytes, int inter,
+                        bool gate_up, cudaStream_t stream);
+
 // Router scores logits[t][e] = W_g[e] . h[t] (fp32 accumulation).
 cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h, int n, int d,
                                  int n_experts, float *logits, cudaStream_t stream);

@@ -13,6 +13,11 @@
 
 namespace moe {
 
+// Geometry of a packed weight tile (pack.cu) = one pipeline stage of the
+// tensor-core expert kernel: 64 rows x 512 bytes, 8 consumer warps x 64 bytes.
+constexpr int PACK_ROWS = 64;
+constexpr int PACK_KBYTES = 512;
+
 // ------------------------------------------------------------------ status
 
 // The first device-side error wins; later ones are dropped.
