@@ -44,7 +44,7 @@ METRIC = "µs per MoE verify pass and union-byte HBM GB/s (% of GB300 peak) vs n
 WORKLOAD = "deepseek-v3-shaped fp8-e4m3 moe layer, n=8 draft-tree tokens (rho=0.6), dedup verify pass"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_PASS = 7  # router scores, top-k, plan, bf16->fp16, gate/up, down, combine
+KERNELS_PER_PASS = 6  # router scores, top-k, plan, gate/up, down, combine
 
 
 def parse():
@@ -241,11 +241,11 @@ def run_ours(args):
     value = ws * union_bytes / (ms_per_step * 1e-3) / 1e9
 
     # algorithmic bytes of one moe_verify_dedup call: union expert bytes + the
-    # hidden states (bf16 read, fp16 copy written and read), the
-    # intermediate a (fp16, written and read once per slot) and the per-slot
-    # fp32 outputs (written, read) + y (bf16) + gate weights
+    # hidden states (bf16, read once), the intermediate a (fp16, written and
+    # read once per slot), the per-slot fp32 outputs (written, read), y (bf16)
+    # and the gate weights
     slots = n * (CFG.top_k + CFG.n_shared)
-    act_bytes = (n * CFG.d * (2 + 2 + 2) + 2 * slots * CFG.inter * 2 + 2 * slots * CFG.d * 4
+    act_bytes = (n * CFG.d * 2 + 2 * slots * CFG.inter * 2 + 2 * slots * CFG.d * 4
                  + n * CFG.d * 2 + n * CFG.top_k * 4)
     alg_bytes = union_bytes + act_bytes
     dedup_avg = statistics.mean(dedup_ms)

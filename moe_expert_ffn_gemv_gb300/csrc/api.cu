@@ -137,11 +137,7 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     if (e == cudaSuccess) e = launch_expert_f32(2, P, 2 * sms, stream);
   } else {
     const bool fp8 = L.w_dtype == MOE_E4M3_B128;
-    const void *act = h;
-    if (fp8) {
-      e = launch_bf16_to_f16(h, wsb + ws.act16, int64_t(n) * L.d, stream);
-      act = wsb + ws.act16;
-    }
+    const void *act = h;  // bf16; the E4M3 kernel converts it to fp16 in registers
     // tokens per segment: at most n (dedup; one per slot for per-slot)
     const int m_max = plan ? n : 1;
     const int n_tiles = m_max <= 8 ? 1 : m_max <= 16 ? 2 : 4;

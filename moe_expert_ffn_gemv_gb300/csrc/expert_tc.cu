@@ -165,6 +165,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   constexpr int ES = FP8 ? 1 : 2;       // bytes per weight element
   constexpr int TOK = 8 * NT;           // tokens per pass over an item
   constexpr int BW = FP8 ? 8 : 4;       // B-fragment words per N tile and stage
+  // E4M3 phase 1 reads the bf16 hidden states and converts them to fp16
+  constexpr bool BF16_ACT_TO_F16 = FP8 && PHASE == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
   float4 *red = reinterpret_cast<float4 *>(smem + S * STAGE_BYTES);
@@ -295,6 +297,16 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
           bfr[nt][4 * v + 2] = x.z;
           bfr[nt][4 * v + 3] = x.w;
         }
+        if (BF16_ACT_TO_F16) {
+          // the hidden states arrive as bf16; the fp16 MMA wants fp16 pairs
+#pragma unroll
+          for (int v = 0; v < BW; ++v) {
+            const uint32_t x = bfr[nt][v];
+            const __half2 h2 =
+                __floats2half2_rn(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+            bfr[nt][v] = *reinterpret_cast<const uint32_t *>(&h2);
+          }
+        }
       }
     }
     sc_a = sc_b = 1.f;
@@ -371,10 +383,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t a[4];
-            a[0] = e4m3x2_to_f16x2(wl[j]);
-            a[1] = e4m3x2_to_f16x2(wh[j]);
-            a[2] = e4m3x2_to_f16x2(wl[j] >> 16);
-            a[3] = e4m3x2_to_f16x2(wh[j] >> 16);
+            e4m3x4_to_f16x2x2(wl[j], a[0], a[2]);
+            e4m3x4_to_f16x2x2(wh[j], a[1], a[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               if (nt * 8 < m_left) mma_16816<false>(tmp[nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);

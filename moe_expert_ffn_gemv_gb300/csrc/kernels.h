@@ -20,7 +20,7 @@ struct TcParams {
   int32_t kdim;           // columns: d (phase 1) or I (phase 2)
   int32_t inter;          // I
   int32_t row_blocks;     // work items per segment: I/32 (phase 1) or d/64 (phase 2)
-  const void *act;        // phase 1: activations [n][d] by token; phase 2: a [slots][I]
+  const void *act;        // phase 1: hidden states [n][d] (bf16) by token; phase 2: a [slots][I]
   void *out;              // phase 1: a [slots][I]; phase 2: yslot [slots][d] fp32
   int32_t *err;           // workspace error word
   uint64_t timeout_ns;    // limit of every wait
@@ -63,9 +63,6 @@ cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, in
                               int64_t expert_bytes, int32_t *hist, int32_t *uniq, int32_t *n_uniq,
                               int32_t *offs, int32_t *perm, int64_t *union_bytes, int32_t *err,
                               cudaStream_t stream);
-
-// bf16 -> fp16 copy of the hidden states (E4M3 path).
-cudaError_t launch_bf16_to_f16(const void *src, void *dst, int64_t count, cudaStream_t stream);
 
 // y[t] = sum_j w[t][j] yslot[t*k+j] (+ yslot[n*k+t]) -> y (fp32 or bf16).
 cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,

@@ -126,22 +126,30 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
   }
 }
 
-// Two E4M3 bytes (low byte first) -> f16x2 (low half = low byte); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 bytes b0..b3 (b0 least significant) -> two f16x2 words:
+// lo = (b0, b1), hi = (b2, b3), the lower byte in the lower half.  Exact:
+// every E4M3 value is an fp16 value.  One cvt per pair, no repacking.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_bytes, uint32_t &lo,
+                                                  uint32_t &hi) {
+  asm("{\n"
+      ".reg .b16 l, h;\n"
+      "mov.b32 {l, h}, %2;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_bytes));
 }
 
 // --------------------------------------------------------------- workspace
 
 // Layout of the caller's workspace (all offsets 256-byte aligned):
 //   [0, 256)           int32 error word (+ padding)
-//   act16              [n_max][d] fp16 copy of h (E4M3 weights only)
 //   inter              [n_max*(k+n_shared)][I] intermediate a = silu(g)*u
+//                      (fp32 for F32 weights, bf16 for BF16, fp16 for E4M3)
 //   yslot              [n_max*(k+n_shared)][d] fp32 per-slot expert outputs
 struct Workspace {
-  size_t act16, inter, yslot, total;
+  size_t inter, yslot, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -151,8 +159,6 @@ inline Workspace workspace_layout(const moe_layer_desc &L) {
   const size_t inter_es = L.w_dtype == MOE_F32 ? 4 : 2;
   Workspace w;
   size_t off = 256;
-  w.act16 = off;
-  off += align256(L.w_dtype == MOE_E4M3_B128 ? size_t(L.n_max) * L.d * 2 : 0);
   w.inter = off;
   off += align256(slots * size_t(L.inter) * inter_es);
   w.yslot = off;

@@ -3,11 +3,12 @@
 // Speculative Decoding", Sec. 2.2, eq. (4): s = W_g h, E(h) = TopK(s, k), the
 // selected scores normalised by softmax or sigmoid).
 //
-//   router_scores_kernel  one CTA per (expert, group of 8 tokens); its 8 warps
-//                         split d, each lane takes 8 contiguous elements
-//                         (16-byte loads of bf16, 2 x 16 bytes of fp32); the
-//                         warps' partial sums are added in a fixed order, so
-//                         the fp32 logits are reproducible run to run.
+//   router_scores_kernel  one CTA per (expert, group of 8 tokens); its warps
+//                         split d in 256-column chunks, each lane takes 8
+//                         contiguous elements (16-byte loads of bf16, 2 x 16
+//                         bytes of fp32); the warps' partial sums are added in
+//                         a fixed order, so the fp32 logits are reproducible
+//                         run to run.
 //   topk_gate_kernel      one warp per token; each lane holds up to 8 of the
 //                         N <= 256 logits; k rounds of a warp arg-max over
 //                         (logit desc, id asc) with xor shuffles pick the
@@ -41,31 +42,38 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
   }
 }
 
+// One CTA per (expert, group of 8 tokens), one warp per 256-column chunk of
+// d (up to 16 warps; larger d loops), so a lane issues its loads together and
+// the whole dot product costs one or two L2 round trips.
+constexpr int ROUTER_MAX_WARPS = 16;
+
 template <typename T>
-__global__ void __launch_bounds__(256) router_scores_kernel(const T *__restrict__ wg,
-                                                            const T *__restrict__ h, int n, int d,
-                                                            int n_experts,
-                                                            float *__restrict__ logits) {
-  __shared__ float part[8][TOKENS_PER_CTA];
+__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) router_scores_kernel(const T *__restrict__ wg,
+                                                             const T *__restrict__ h, int n, int d,
+                                                             int n_experts,
+                                                             float *__restrict__ logits) {
+  __shared__ float part[ROUTER_MAX_WARPS][TOKENS_PER_CTA];
   const int e = blockIdx.x;
   const int t0 = blockIdx.y * TOKENS_PER_CTA;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_warps = blockDim.x >> 5;
   const int nt = min(TOKENS_PER_CTA, n - t0);
   float acc[TOKENS_PER_CTA];
 #pragma unroll
   for (int t = 0; t < TOKENS_PER_CTA; ++t) acc[t] = 0.f;
-  for (int c = threadIdx.x * 8; c < d; c += 256 * 8) {
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float wv[8];
     load8(wg + int64_t(e) * d + c, wv);
+    float hv[TOKENS_PER_CTA][8];
 #pragma unroll
-    for (int t = 0; t < TOKENS_PER_CTA; ++t) {
+    for (int t = 0; t < TOKENS_PER_CTA; ++t)
+      if (t < nt) load8(h + int64_t(t0 + t) * d + c, hv[t]);
+#pragma unroll
+    for (int t = 0; t < TOKENS_PER_CTA; ++t)
       if (t < nt) {
-        float hv[8];
-        load8(h + int64_t(t0 + t) * d + c, hv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[t] = fmaf(wv[i], hv[i], acc[t]);
+        for (int i = 0; i < 8; ++i) acc[t] = fmaf(wv[i], hv[t][i], acc[t]);
       }
-    }
   }
 #pragma unroll
   for (int t = 0; t < TOKENS_PER_CTA; ++t) {
@@ -77,8 +85,7 @@ __global__ void __launch_bounds__(256) router_scores_kernel(const T *__restrict_
   __syncthreads();
   if (threadIdx.x < nt) {
     float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) s += part[w][threadIdx.x];
+    for (int w = 0; w < n_warps; ++w) s += part[w][threadIdx.x];
     logits[int64_t(t0 + threadIdx.x) * n_experts + e] = s;
   }
 }
@@ -167,14 +174,16 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict_
 cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h, int n, int d,
                                  int n_experts, float *logits, cudaStream_t stream) {
   dim3 grid(n_experts, (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
+  int warps = (d + 255) / 256;
+  warps = warps < 1 ? 1 : warps > ROUTER_MAX_WARPS ? ROUTER_MAX_WARPS : warps;
   if (bf16)
-    router_scores_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+    router_scores_kernel<__nv_bfloat16><<<grid, warps * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(router_w), static_cast<const __nv_bfloat16 *>(h), n, d,
         n_experts, logits);
   else
-    router_scores_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(router_w),
-                                                          static_cast<const float *>(h), n, d,
-                                                          n_experts, logits);
+    router_scores_kernel<float><<<grid, warps * 32, 0, stream>>>(
+        static_cast<const float *>(router_w), static_cast<const float *>(h), n, d, n_experts,
+        logits);
   return cudaGetLastError();
 }
 
