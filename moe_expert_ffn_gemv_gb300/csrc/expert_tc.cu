@@ -35,9 +35,11 @@
 //     single 128x128 scale block;
 //   - the activation fragments and scales of the next stage are loaded while
 //     the current stage computes; the plan sits in shared memory;
-//   - after the last stage of an item the 8 warps' partial sums are added in
-//     shared memory in a fixed order (deterministic), and the epilogue applies
-//     silu(g)*u (phase 1) or stores the fp32 rows (phase 2).
+//   - after the last stage of an item each consumer warp drops its partial
+//     sums into one of two reduction buffers and goes on streaming; warp 9,
+//     the epilogue warp, adds the 8 warps' partials in a fixed order
+//     (deterministic) and applies silu(g)*u (phase 1) or stores the fp32 rows
+//     (phase 2), so no consumer waits for another at item boundaries.
 // Every wait is bounded; on time-out the kernel records MOE_ERR_TIMEOUT in the
 // workspace error word, keeps its barrier structure, lets its own copies land
 // and returns.
@@ -51,23 +53,27 @@ namespace {
 constexpr int ROWS = PACK_ROWS;      // weight rows per stage (4 MMA row tiles)
 constexpr int KBYTES = PACK_KBYTES;  // bytes of each row per stage
 constexpr int STAGE_BYTES = ROWS * KBYTES;
-constexpr int CONSUMERS = 8;
-constexpr int THREADS = (CONSUMERS + 1) * 32;
+constexpr int CONSUMERS = 8;                      // warps 0..7
+constexpr int PRODUCER = CONSUMERS;                // warp 8
+constexpr int EPILOGUE = CONSUMERS + 1;            // warp 9
+constexpr int THREADS = (CONSUMERS + 2) * 32;
 constexpr uint64_t DRAIN_LIMIT_NS = 200ull * 1000 * 1000;
 
+// Shared memory: the weight ring, then the cross-warp reduction buffers
+// (consumers hand an item's partial sums to the epilogue warp there).
 template <int NT>
-constexpr int n_stages() { return NT >= 4 ? 4 : NT == 2 ? 5 : 6; }
+constexpr int n_red_bufs() { return NT >= 4 ? 1 : 2; }
 
 template <int NT>
 constexpr size_t red_bytes() { return size_t(CONSUMERS) * 4 * NT * 32 * 16; }
 
 template <int NT>
-constexpr size_t smem_bytes() {
-  return size_t(n_stages<NT>()) * STAGE_BYTES + red_bytes<NT>() + 2 * n_stages<NT>() * 8;
-}
+constexpr int n_stages() { return NT >= 4 ? 4 : NT == 2 ? 4 : 5; }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+template <int NT>
+constexpr size_t smem_bytes() {
+  return size_t(n_stages<NT>()) * STAGE_BYTES + n_red_bufs<NT>() * red_bytes<NT>() +
+         2 * (n_stages<NT>() + n_red_bufs<NT>()) * 8;
 }
 
 __device__ __forceinline__ float silu_times(float g, float u) {
@@ -162,6 +168,7 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
 template <bool FP8, int PHASE, int NT>
 __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P) {
   constexpr int S = n_stages<NT>();
+  constexpr int RB = n_red_bufs<NT>();
   constexpr int ES = FP8 ? 1 : 2;       // bytes per weight element
   constexpr int TOK = 8 * NT;           // tokens per pass over an item
   constexpr int BW = FP8 ? 8 : 4;       // B-fragment words per N tile and stage
@@ -169,9 +176,12 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   constexpr bool BF16_ACT_TO_F16 = FP8 && PHASE == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
-  float4 *red = reinterpret_cast<float4 *>(smem + S * STAGE_BYTES);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * STAGE_BYTES + red_bytes<NT>());
+  float4 *red = reinterpret_cast<float4 *>(smem + S * STAGE_BYTES);   // [RB][red_bytes]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * STAGE_BYTES + RB * red_bytes<NT>());
   uint64_t *empty = full + S;
+  uint64_t *rfull = empty + S;    // consumers -> epilogue warp (count CONSUMERS)
+  uint64_t *rempty = rfull + RB;  // epilogue warp -> consumers (count 1)
+  constexpr int RED_F4 = int(red_bytes<NT>() / 16);
   __shared__ volatile int s_abort;
   __shared__ int32_t s_uniq[MAX_EXPERTS];
   __shared__ int32_t s_offs[MAX_EXPERTS + 1];
@@ -184,6 +194,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], CONSUMERS);
+    }
+    for (int b = 0; b < RB; ++b) {
+      mbar_init(&rfull[b], CONSUMERS);
+      mbar_init(&rempty[b], 1);
     }
     s_abort = 0;
     s_U = P.T.dedup ? *P.T.n_uniq : 0;
@@ -207,7 +221,75 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   const int scale_cols = P.kdim / 128;              // E4M3 scale table width
   const int64_t scale_stride = int64_t(P.rows_total / 128) * scale_cols;
 
-  if (warp == CONSUMERS) {
+  if (warp == EPILOGUE) {
+    // -------------------------------------------------------------- epilogue
+    // For each (item, token group), in the consumers' order: add the 8 warps'
+    // K-partials in a fixed order, then silu(g)*u (phase 1) or the fp32 rows
+    // (phase 2), and give the buffer back.
+    bool aborted = false;
+    uint32_t ep = 0;
+    Cursor cur;
+    cur.item = blockIdx.x;
+    bool have = cursor_item<TOK>(cur, T, n_items, P.row_blocks, P.err, false);
+    while (have) {
+      const int b = ep % RB;
+      const uint32_t round = ep / RB;
+      if (!aborted && s_abort) aborted = true;
+      if (!aborted && !mbar_wait_bounded(&rfull[b], round & 1, P.timeout_ns)) {
+        aborted = true;
+        s_abort = 1;
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+      }
+      if (!aborted) {
+        const float4 *rb_buf = red + b * RED_F4;
+        const int m_left = cur.sg.m - cur.grp * TOK;
+        constexpr int MT_OUT = PHASE == 1 ? 2 : 4;
+        for (int q = lane; q < MT_OUT * NT * 32; q += 32) {
+          const int ln = q & 31, nt = (q >> 5) % NT, mt = q / (32 * NT);
+          if (nt * 8 >= m_left) continue;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f), w4 = v;
+#pragma unroll
+          for (int w = 0; w < CONSUMERS; ++w) {
+            const float4 x = rb_buf[((w * 4 + mt) * NT + nt) * 32 + ln];
+            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+            if (PHASE == 1) {
+              const float4 y = rb_buf[((w * 4 + mt + 2) * NT + nt) * 32 + ln];
+              w4.x += y.x; w4.y += y.y; w4.z += y.z; w4.w += y.w;
+            }
+          }
+          const int gg = ln >> 2, cc = ln & 3;
+          const float vals[4] = {v.x, v.y, v.z, v.w};
+          const float ups[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = mt * 16 + gg + (e >> 1) * 8;
+            const int col = nt * 8 + 2 * cc + (e & 1);
+            if (col >= m_left) continue;
+            const int slot = T.slot(cur.sg, cur.grp * TOK + col);
+            if (PHASE == 1) {
+              const float a = silu_times(vals[e], ups[e]);
+              uint16_t *out =
+                  static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter + cur.rb * 32 + row;
+              if (FP8) *reinterpret_cast<__half *>(out) = __float2half_rn(a);
+              else *reinterpret_cast<__nv_bfloat16 *>(out) = __float2bfloat16_rn(a);
+            } else {
+              float *out = static_cast<float *>(P.out) + int64_t(slot) * P.rows_total +
+                           cur.rb * ROWS + row;
+              *out = vals[e];
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[b]);
+      ++ep;
+      cur.ks = kstages - 1;  // step to the next (item, token group)
+      have = cursor_next<TOK>(cur, T, n_items, P.row_blocks, kstages, P.err, false);
+    }
+    return;
+  }
+
+  if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = policy_evict_first();
     uint32_t it = 0;
@@ -260,6 +342,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   const int tid = threadIdx.x;
   const uint16_t *act = static_cast<const uint16_t *>(P.act);
   uint32_t it = 0;
+  uint32_t ep = 0;  // (item, token group)s handed to the epilogue warp
   bool aborted = false;
 
   // activation row of this lane's token in each N tile (-1: none)
@@ -296,16 +379,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
           bfr[nt][4 * v + 1] = x.y;
           bfr[nt][4 * v + 2] = x.z;
           bfr[nt][4 * v + 3] = x.w;
-        }
-        if (BF16_ACT_TO_F16) {
-          // the hidden states arrive as bf16; the fp16 MMA wants fp16 pairs
-#pragma unroll
-          for (int v = 0; v < BW; ++v) {
-            const uint32_t x = bfr[nt][v];
-            const __half2 h2 =
-                __floats2half2_rn(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-            bfr[nt][v] = *reinterpret_cast<const uint32_t *>(&h2);
-          }
         }
       }
     }
@@ -365,39 +438,68 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       s_abort = 1;
       if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
     }
+    if (BF16_ACT_TO_F16) {
+      // the hidden states arrive as bf16 (loaded a stage ago); the fp16 MMA
+      // wants fp16 pairs
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int v = 0; v < BW; ++v) {
+          const uint32_t x = bfr[nt][v];
+          const __half2 h2 =
+              __floats2half2_rn(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+          bfr[nt][v] = *reinterpret_cast<const uint32_t *>(&h2);
+        }
+    }
     if (!aborted && active) {
-      // this warp's 4 KB of the stage: [row tile mt][half h][lane][16 bytes]
+      // this warp's 4 KB of the stage: [row tile mt][half h][lane][16 bytes];
+      // all of it first, then the MMAs with the four row tiles' chains
+      // interleaved (consecutive MMAs are independent)
       const uint4 *st = reinterpret_cast<const uint4 *>(ring + s * STAGE_BYTES) + warp * 256 + lane;
+      uint32_t wl[4][4], wh[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const uint4 lo = st[(mt * 2 + 0) * 32];
         const uint4 hi = st[(mt * 2 + 1) * 32];
-        const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w};
-        const uint32_t wh[4] = {hi.x, hi.y, hi.z, hi.w};
-        if (FP8) {
-          float tmp[NT][4];
+        wl[mt][0] = lo.x; wl[mt][1] = lo.y; wl[mt][2] = lo.z; wl[mt][3] = lo.w;
+        wh[mt][0] = hi.x; wh[mt][1] = hi.y; wh[mt][2] = hi.z; wh[mt][3] = hi.w;
+      }
+      if (FP8) {
+        float tmp[4][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmp[nt][q] = 0.f;
+            for (int q = 0; q < 4; ++q) tmp[mt][nt][q] = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
             uint32_t a[4];
-            e4m3x4_to_f16x2x2(wl[j], a[0], a[2]);
-            e4m3x4_to_f16x2x2(wh[j], a[1], a[3]);
+            e4m3x4_to_f16x2x2(wl[mt][j], a[0], a[2]);
+            e4m3x4_to_f16x2x2(wh[mt][j], a[1], a[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              if (nt * 8 < m_left) mma_16816<false>(tmp[nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);
+              if (nt * 8 < m_left)
+                mma_16816<false>(tmp[mt][nt], a, bfr[nt][2 * j], bfr[nt][2 * j + 1]);
           }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
           const float scl = mt < 2 ? sc_a : sc_b;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[mt][nt][q] = fmaf(scl, tmp[nt][q], acc[mt][nt][q]);
-        } else {
+            for (int q = 0; q < 4; ++q) acc[mt][nt][q] = fmaf(scl, tmp[mt][nt][q], acc[mt][nt][q]);
+        }
+      } else {
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint32_t a[4] = {wl[2 * j], wh[2 * j], wl[2 * j + 1], wh[2 * j + 1]};
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t a[4] = {wl[mt][2 * j], wh[mt][2 * j], wl[mt][2 * j + 1],
+                                   wh[mt][2 * j + 1]};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               if (nt * 8 < m_left)
@@ -411,53 +513,27 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     ++it;
 
     if (cur.ks == kstages - 1) {
-      // ---- epilogue of (item, token group): add the 8 warps' K-partials in
-      // a fixed order, then silu(g)*u (phase 1) or the fp32 rows (phase 2)
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          red[((warp * 4 + mt) * NT + nt) * 32 + lane] =
-              make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
-      consumer_sync();
-      if (!aborted) {
-        constexpr int MT_OUT = PHASE == 1 ? 2 : 4;
-        for (int q = tid; q < MT_OUT * NT * 32; q += CONSUMERS * 32) {
-          const int ln = q & 31, nt = (q >> 5) % NT, mt = q / (32 * NT);
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f), w4 = v;
-#pragma unroll
-          for (int w = 0; w < CONSUMERS; ++w) {
-            const float4 x = red[((w * 4 + mt) * NT + nt) * 32 + ln];
-            v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
-            if (PHASE == 1) {
-              const float4 y = red[((w * 4 + mt + 2) * NT + nt) * 32 + ln];
-              w4.x += y.x; w4.y += y.y; w4.z += y.z; w4.w += y.w;
-            }
-          }
-          const int gg = ln >> 2, cc = ln & 3;
-          const float vals[4] = {v.x, v.y, v.z, v.w};
-          const float ups[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = mt * 16 + gg + (e >> 1) * 8;
-            const int col = nt * 8 + 2 * cc + (e & 1);
-            if (col >= m_left) continue;
-            const int slot = T.slot(cur.sg, cur.grp * TOK + col);
-            if (PHASE == 1) {
-              const float a = silu_times(vals[e], ups[e]);
-              uint16_t *out =
-                  static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter + cur.rb * 32 + row;
-              if (FP8) *reinterpret_cast<__half *>(out) = __float2half_rn(a);
-              else *reinterpret_cast<__nv_bfloat16 *>(out) = __float2bfloat16_rn(a);
-            } else {
-              float *out = static_cast<float *>(P.out) + int64_t(slot) * P.rows_total +
-                           cur.rb * ROWS + row;
-              *out = vals[e];
-            }
-          }
-        }
+      // hand this (item, token group)'s K-partials to the epilogue warp
+      const int b = ep % RB;
+      const uint32_t round = ep / RB;
+      if (!aborted && s_abort) aborted = true;
+      if (!aborted && round > 0 && !mbar_wait_bounded(&rempty[b], (round - 1) & 1, P.timeout_ns)) {
+        aborted = true;
+        s_abort = 1;
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
       }
-      consumer_sync();
+      if (!aborted) {
+        float4 *rb_buf = red + b * RED_F4;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            rb_buf[((warp * 4 + mt) * NT + nt) * 32 + lane] =
+                make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[b]);
+      ++ep;
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
