@@ -220,6 +220,35 @@ moe_status moe_verify_perslot(const moe_layer_desc *desc,
 moe_status moe_workspace_init(void *workspace, size_t ws_bytes,
                               moe_stream_t stream);
 
+/* moe_verify_dedup for callers that cannot provide a workspace.
+ *
+ * No counterpart on the pages: this exists for callers that may not allocate
+ * device memory themselves, e.g. code whose device memory belongs to a
+ * framework allocator it must not go around, or a latency-critical path that
+ * must never call cudaMalloc (which can synchronise the device and may fail
+ * where nothing can recover).  It computes the same output as
+ * moe_verify_dedup with the same arguments, but its scratch (error word,
+ * intermediate activations, per-slot outputs) is a fixed 16 MiB array inside
+ * the library, held on every GPU that loads the library until the process
+ * exits; the call itself allocates and frees nothing.
+ *   - Limit: the scratch for n tokens must fit 16 MiB, i.e.
+ *     256 + n*(k + n_shared)*(I*e + 4*d) bytes (each part rounded up to
+ *     256 bytes; e = 4 for F32 weights, else 2); a larger call returns
+ *     MOE_ERR_WORKSPACE and enqueues nothing (DeepSeek-V3 shapes: n <= 56).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array: calls whose execution may overlap on the
+ *     GPU (other streams, other host threads) race; serialise them.
+ *   - error_word: device int32 (4-byte aligned) that receives the call's
+ *     device-side status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_INPUT)
+ *     once the call's work completes on `stream`; may be NULL. */
+moe_status moe_verify_dedup_noalloc(const moe_layer_desc *desc,
+                                    const moe_expert_weights *weights,
+                                    const void *h, int32_t n,
+                                    const int32_t *ids, const float *w,
+                                    const moe_plan *plan, void *y,
+                                    int32_t *error_word, moe_stream_t stream);
+
 /* Synchronises `stream`, then returns (and clears) the first error that a
  * kernel recorded in the workspace's error word: MOE_OK, MOE_ERR_TIMEOUT or
  * MOE_ERR_DEVICE_INPUT; MOE_ERR_CUDA if the synchronisation itself failed. */

@@ -34,7 +34,7 @@ MOE_GATE_SOFTMAX, MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1, 2
 EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_topk_from_logits",
             "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot", "moe_workspace_init",
             "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
-            "moe_pack_expert_weights"]
+            "moe_pack_expert_weights", "moe_verify_dedup_noalloc"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -71,6 +71,9 @@ _lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ct
 _lib.moe_verify_perslot.restype = ctypes.c_int
 _lib.moe_verify_perslot.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32,
                                     _P, _P, _P, ctypes.c_size_t, _P, _P]
+_lib.moe_verify_dedup_noalloc.restype = ctypes.c_int
+_lib.moe_verify_dedup_noalloc.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32,
+                                          _P, _P, ctypes.POINTER(moe_plan), _P, _P, _P]
 _lib.moe_pack_expert_weights.restype = ctypes.c_int
 _lib.moe_pack_expert_weights.argtypes = [_D, _P, _P, ctypes.c_int32, _P, _P, _P]
 _lib.moe_workspace_init.restype = ctypes.c_int
@@ -143,6 +146,16 @@ def moe_verify_dedup(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_
                                  _ptr(w), ctypes.byref(plan), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _ptr(y),
                                  _stream(stream)), "moe_verify_dedup")
+
+
+def moe_verify_dedup_noalloc(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_plan, y,
+                             error_word=None, stream=None) -> None:
+    """The deduplicating pass with the library's own fixed scratch (no
+    workspace): for callers that cannot allocate device memory themselves."""
+    _check(_lib.moe_verify_dedup_noalloc(ctypes.byref(desc), ctypes.byref(weights), _ptr(h), n,
+                                         _ptr(ids), _ptr(w), ctypes.byref(plan), _ptr(y),
+                                         _ptr(error_word), _stream(stream)),
+           "moe_verify_dedup_noalloc")
 
 
 def moe_verify_perslot(desc, weights: moe_expert_weights, h, n, ids, w, workspace, y,

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "kernels.h"
 #include "moe_common.cuh"
 
@@ -309,6 +311,78 @@ MOE_API moe_status moe_verify_perslot(const moe_layer_desc *desc,
   if (n == 0) return MOE_OK;
   return run_experts(*desc, *weights, h, n, ids, w, nullptr, workspace, y,
                      static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Deduplicating pass without caller-provided scratch.
+//
+// For callers that cannot hand the library a workspace: code whose device
+// memory is owned by a framework allocator it may not bypass, or a hot path
+// that must never call cudaMalloc (which can synchronise the device and whose
+// failure it could not handle there).  The scratch of such a call lives in
+// this fixed, file-scope device array, which every GPU that loads the library
+// keeps until the process exits.  All calls share it: it holds whatever the
+// last call left, so calls whose execution overlaps on the GPU (e.g. on two
+// streams, or from two threads) race and must be serialised by the caller.
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[NOALLOC_MAX_DEVICES] = {nullptr};
+
+// The array's device address on the current device, looked up once per
+// device (host code only holds a stand-in symbol, not a usable address).
+moe_status noalloc_scratch(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES)
+    return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return MOE_OK;
+}
+}  // namespace
+
+MOE_API moe_status moe_verify_dedup_noalloc(const moe_layer_desc *desc,
+                                            const moe_expert_weights *weights, const void *h,
+                                            int32_t n, const int32_t *ids, const float *w,
+                                            const moe_plan *plan, void *y, int32_t *error_word,
+                                            moe_stream_t stream) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  s = check_weights(*desc, weights);
+  if (s != MOE_OK) return s;
+  if (!h || !ids || !w || !y || !plan || !plan->uniq || !plan->offs || !plan->perm ||
+      !plan->n_uniq)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(ids) || !aligned16(w) || !aligned16(y) ||
+      (error_word && (reinterpret_cast<uintptr_t>(error_word) & 3u)))
+    return MOE_ERR_ALIGNMENT;
+  // the scratch this call needs, laid out for exactly n tokens
+  moe_layer_desc L = *desc;
+  L.n_max = n;
+  if (workspace_layout(L).total > NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the error word must start at zero; the rest is fully written before it is read
+  if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
+  s = run_experts(L, *weights, h, n, ids, w, plan, scratch, y, st);
+  if (s != MOE_OK) return s;
+  if (error_word &&
+      cudaMemcpyAsync(error_word, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 MOE_API moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const void *w13,
