@@ -309,6 +309,28 @@ class VerifyLayer:
             return self.dedup(h, n, y)
         return self.perslot(h, n, y)
 
+    def capture(self, h: torch.Tensor, n: int, engine: str = "dedup"):
+        """Record one verification pass (route, plan, experts, combine) on `h`
+        (a fixed device buffer) into CUDA graphs; returns (route_and_plan,
+        experts), two torch.cuda.CUDAGraph objects replayed in that order.
+        Every call of the pass is asynchronous and host-sync free, so it can
+        be captured; replays read whatever `h` holds and write self.y."""
+        # one eager pass first: sets kernel attributes and warms the library
+        self.verify_pass(h, n, engine)
+        torch.cuda.synchronize()
+        g_route = torch.cuda.CUDAGraph()
+        g_experts = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_route):
+            self.route(h, n)
+            if engine == "dedup":
+                self.union_plan(n)
+        with torch.cuda.graph(g_experts):
+            if engine == "dedup":
+                self.dedup(h, n)
+            else:
+                self.perslot(h, n)
+        return g_route, g_experts
+
     def last_error(self) -> int:
         return moe_last_error(self.workspace)
 

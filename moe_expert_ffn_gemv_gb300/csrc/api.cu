@@ -140,9 +140,11 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
   } else {
     const bool fp8 = L.w_dtype == MOE_E4M3_B128;
     const void *act = h;  // bf16; the E4M3 kernel converts it to fp16 in registers
-    // tokens per segment: at most n (dedup; one per slot for per-slot)
-    const int m_max = plan ? n : 1;
-    const int n_tiles = m_max <= 8 ? 1 : m_max <= 16 ? 2 : 4;
+    // One 8-token MMA tile per pass over a work item: a segment with more
+    // tokens (the shared expert has all n) takes several passes over its
+    // weights.  Wider tiles (2 or 4 per pass) run out of registers and
+    // reduction buffers and measure slower than the re-read costs.
+    const int n_tiles = 1;
     TcParams P;
     P.T = T;
     P.err = err;

@@ -559,17 +559,26 @@ template <bool FP8, int PHASE, int NT>
 cudaError_t launch_one(const TcParams &P, int grid, cudaStream_t stream) {
   auto kern = expert_tc_kernel<FP8, PHASE, NT>;
   const size_t smem = smem_bytes<NT>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  // the shared-memory opt-in is set once per device (the first call), so
+  // later calls, e.g. under stream capture, only launch
+  static unsigned long long configured = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (!(configured & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
   kern<<<grid, THREADS, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
 template <bool FP8, int PHASE>
 cudaError_t launch_nt(const TcParams &P, int nt, int grid, cudaStream_t stream) {
-  if (nt <= 1) return launch_one<FP8, PHASE, 1>(P, grid, stream);
-  if (nt == 2) return launch_one<FP8, PHASE, 2>(P, grid, stream);
-  return launch_one<FP8, PHASE, 4>(P, grid, stream);
+  if (nt != 1) return cudaErrorInvalidValue;  // only the 8-token tile is built
+  return launch_one<FP8, PHASE, 1>(P, grid, stream);
 }
 
 }  // namespace

@@ -73,3 +73,23 @@ def test_out_of_range_ids_are_reported_by_both_engines(mv):
     vl.union_plan(n)
     vl.dedup(h, n)
     assert vl.last_error() == mv.MOE_OK
+
+
+def test_pass_replays_from_a_cuda_graph(mv):
+    # the pass is host-sync free: captured once, replays match the eager pass
+    cfg = synth.LayerConfig("fp8-graph", 640, 10, 4, 384, synth.BF16, synth.E4M3,
+                            synth.GATE_SIGMOID_RENORM, n_shared=1)
+    layer = synth.make_layer(cfg, seed=8).to("cuda")
+    n = 12
+    vl = mv.VerifyLayer(layer, n)
+    h = torch.empty(n, cfg.d, dtype=torch.bfloat16, device="cuda")
+    h.copy_(synth.make_hidden(cfg, n, seed=9))
+    g_route, g_exp = vl.capture(h, n)
+    for seed in (10, 11):
+        h.copy_(synth.make_hidden(cfg, n, seed=seed))
+        g_route.replay()
+        g_exp.replay()
+        y_graph = vl.y[:n].clone()
+        y_eager = vl.verify_pass(h, n).clone()
+        assert vl.last_error() == mv.MOE_OK
+        assert torch.equal(y_graph, y_eager)
