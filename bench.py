@@ -6,9 +6,10 @@ block scales), n = 8 draft-tree tokens (BFS tree, 4 children under the root,
 2 below; child = 0.6 parent + 0.8 eps).  Synthetic, seeded weights and
 hidden states; weights resident in HBM.
 
-One step = one verification pass through the C ABI: router scores + top-k
-(moe_route_topk), union plan (moe_union_plan), the deduplicating expert FFN
-and combine (moe_verify_dedup), recorded once into CUDA graphs and replayed.  `value` = union-expert bytes per pass
+One step = one verification pass through the C ABI: router scores, top-k
+and union plan in one launch (moe_route_plan), then the deduplicating expert
+FFN and combine (moe_verify_dedup), recorded once into CUDA graphs and
+replayed.  `value` = union-expert bytes per pass
 (routed union + shared expert, weights and scales) / device time per pass.
 The expert bytes of one pass (~2.5 GB) exceed the 129 MB L2, so passes run
 back to back with no flush.
@@ -44,7 +45,7 @@ METRIC = "µs per MoE verify pass and union-byte HBM GB/s (% of GB300 peak) vs n
 WORKLOAD = "deepseek-v3-shaped fp8-e4m3 moe layer, n=8 draft-tree tokens (rho=0.6), dedup verify pass"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_PASS = 6  # router scores, top-k, plan, gate/up, down, combine
+KERNELS_PER_PASS = 4  # route + top-k + plan (fused), gate/up, down, combine
 
 
 def parse():

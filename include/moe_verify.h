@@ -187,6 +187,19 @@ moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids,
                           int32_t n, const moe_plan *plan, int32_t *error_word,
                           moe_stream_t stream);
 
+/* moe_route_topk followed by moe_union_plan, in one kernel launch: the
+ * router CTAs write the scores; the last CTA to finish selects the top-k of
+ * every token, gates, and builds the plan.  Same outputs, bit for bit.
+ *   workspace  a workspace initialised by moe_workspace_init (only its
+ *              256-byte header is used: the error word, and a ticket counter
+ *              the kernel leaves at zero); ws_bytes >= 256.  Calls sharing a
+ *              workspace must not overlap on the GPU.
+ * n may be 0: the plan becomes empty (U = 0). */
+moe_status moe_route_plan(const moe_layer_desc *desc, const void *router_w,
+                          const void *h, int32_t n, int32_t *ids, float *w,
+                          float *logits, const moe_plan *plan, void *workspace,
+                          size_t ws_bytes, moe_stream_t stream);
+
 /* The layer output with the deduplicating engine: every expert of the plan
  * (plus the shared expert) is applied once to all tokens routed to it, its
  * weights streamed from HBM once per pass, and

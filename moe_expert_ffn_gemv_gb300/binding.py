@@ -34,7 +34,7 @@ MOE_GATE_SOFTMAX, MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1, 2
 EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_topk_from_logits",
             "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot", "moe_workspace_init",
             "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
-            "moe_pack_expert_weights", "moe_verify_dedup_noalloc"]
+            "moe_pack_expert_weights", "moe_verify_dedup_noalloc", "moe_route_plan"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -65,6 +65,9 @@ _lib.moe_topk_from_logits.restype = ctypes.c_int
 _lib.moe_topk_from_logits.argtypes = [_D, _P, ctypes.c_int32, _P, _P, _P]
 _lib.moe_union_plan.restype = ctypes.c_int
 _lib.moe_union_plan.argtypes = [_D, _P, ctypes.c_int32, ctypes.POINTER(moe_plan), _P, _P]
+_lib.moe_route_plan.restype = ctypes.c_int
+_lib.moe_route_plan.argtypes = [_D, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.POINTER(moe_plan), _P,
+                                ctypes.c_size_t, _P]
 _lib.moe_verify_dedup.restype = ctypes.c_int
 _lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32, _P,
                                   _P, ctypes.POINTER(moe_plan), _P, ctypes.c_size_t, _P, _P]
@@ -138,6 +141,14 @@ def moe_topk_from_logits(desc, logits, n, ids, w, stream=None) -> None:
 def moe_union_plan(desc, ids, n, plan: moe_plan, error_word=None, stream=None) -> None:
     _check(_lib.moe_union_plan(ctypes.byref(desc), _ptr(ids), n, ctypes.byref(plan),
                                _ptr(error_word), _stream(stream)), "moe_union_plan")
+
+
+def moe_route_plan(desc, router_w, h, n, ids, w, logits, plan: moe_plan, workspace,
+                   stream=None) -> None:
+    _check(_lib.moe_route_plan(ctypes.byref(desc), _ptr(router_w), _ptr(h), n, _ptr(ids), _ptr(w),
+                               _ptr(logits), ctypes.byref(plan), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_route_plan")
 
 
 def moe_verify_dedup(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_plan, workspace,
@@ -289,6 +300,11 @@ class VerifyLayer:
     def union_plan(self, n: int) -> None:
         moe_union_plan(self.desc, self.ids, n, self._cplan, self.error_word)
 
+    def route_plan(self, h: torch.Tensor, n: int) -> None:
+        """route + union_plan in one launch."""
+        moe_route_plan(self.desc, self.layer.wg, h, n, self.ids, self.w, self.logits, self._cplan,
+                       self.workspace)
+
     def dedup(self, h: torch.Tensor, n: int, y: Optional[torch.Tensor] = None) -> torch.Tensor:
         y = self.y if y is None else y
         moe_verify_dedup(self.desc, self.weights, h, n, self.ids, self.w, self._cplan,
@@ -303,10 +319,10 @@ class VerifyLayer:
     def verify_pass(self, h: torch.Tensor, n: int, engine: str = "dedup",
                     y: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Route, plan and run the experts: one MoE verification pass."""
-        self.route(h, n)
         if engine == "dedup":
-            self.union_plan(n)
+            self.route_plan(h, n)
             return self.dedup(h, n, y)
+        self.route(h, n)
         return self.perslot(h, n, y)
 
     def capture(self, h: torch.Tensor, n: int, engine: str = "dedup"):
@@ -321,9 +337,10 @@ class VerifyLayer:
         g_route = torch.cuda.CUDAGraph()
         g_experts = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_route):
-            self.route(h, n)
             if engine == "dedup":
-                self.union_plan(n)
+                self.route_plan(h, n)
+            else:
+                self.route(h, n)
         with torch.cuda.graph(g_experts):
             if engine == "dedup":
                 self.dedup(h, n)

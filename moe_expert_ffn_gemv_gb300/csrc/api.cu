@@ -291,6 +291,40 @@ MOE_API moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids
                                        static_cast<cudaStream_t>(stream)));
 }
 
+MOE_API moe_status moe_route_plan(const moe_layer_desc *desc, const void *router_w, const void *h,
+                                  int32_t n, int32_t *ids, float *w, float *logits,
+                                  const moe_plan *plan, void *workspace, size_t ws_bytes,
+                                  moe_stream_t stream) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if (!plan || !plan->hist || !plan->uniq || !plan->n_uniq || !plan->offs || !plan->perm ||
+      !plan->union_bytes || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(plan->hist) || !aligned16(plan->uniq) || !aligned16(plan->offs) ||
+      !aligned16(plan->perm) || !aligned16(workspace))
+    return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  int64_t wb, sb;
+  expert_bytes(*desc, &wb, &sb);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t *wsb = static_cast<uint8_t *>(workspace);
+  int32_t *err = reinterpret_cast<int32_t *>(wsb);
+  if (n == 0)  // the empty plan: U = 0, offs[0] = 0
+    return cuda_status(launch_union_plan(nullptr, 0, desc->n_experts, desc->n_shared, wb + sb,
+                                         plan->hist, plan->uniq, plan->n_uniq, plan->offs,
+                                         plan->perm, plan->union_bytes, err, st));
+  if (!router_w || !h || !ids || !w || !logits) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(router_w) || !aligned16(h) || !aligned16(ids) || !aligned16(w) ||
+      !aligned16(logits))
+    return MOE_ERR_ALIGNMENT;
+  return cuda_status(launch_route_plan(
+      desc->act_dtype == MOE_BF16, router_w, h, n, desc->d, desc->n_experts, desc->top_k,
+      desc->gate, desc->n_shared, wb + sb, logits, ids, w, plan->hist, plan->uniq, plan->n_uniq,
+      plan->offs, plan->perm, plan->union_bytes, err,
+      reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET), st));
+}
+
 MOE_API moe_status moe_verify_dedup(const moe_layer_desc *desc, const moe_expert_weights *weights,
                                     const void *h, int32_t n, const int32_t *ids, const float *w,
                                     const moe_plan *plan, void *workspace, size_t ws_bytes,

@@ -58,6 +58,14 @@ cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h,
 cudaError_t launch_topk_gate(const float *logits, int n, int n_experts, int k, int gate,
                              int32_t *ids, float *w, cudaStream_t stream);
 
+// Router scores + top-k + gate + union plan in one launch; `counter` is a
+// zeroed device word that the kernel leaves zeroed.
+cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, int n, int d,
+                              int n_experts, int k, int gate, int n_shared, int64_t expert_bytes,
+                              float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
+                              int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
+                              int32_t *err, unsigned int *counter, cudaStream_t stream);
+
 // Expert union and slot permutation (one CTA).
 cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, int n_shared,
                               int64_t expert_bytes, int32_t *hist, int32_t *uniq, int32_t *n_uniq,

@@ -145,7 +145,8 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_bytes, uint32_t 
 // --------------------------------------------------------------- workspace
 
 // Layout of the caller's workspace (all offsets 256-byte aligned):
-//   [0, 256)           int32 error word (+ padding)
+//   [0, 256)           header: int32 error word at byte 0, the fused
+//                      route + plan kernel's ticket counter at byte 64
 //   inter              [n_max*(k+n_shared)][I] intermediate a = silu(g)*u
 //                      (fp32 for F32 weights, bf16 for BF16, fp16 for E4M3)
 //   yslot              [n_max*(k+n_shared)][d] fp32 per-slot expert outputs
@@ -154,6 +155,8 @@ struct Workspace {
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr size_t WS_TICKET_OFFSET = 64;
 
 inline Workspace workspace_layout(const moe_layer_desc &L) {
   const size_t slots = size_t(L.n_max) * size_t(L.top_k + L.n_shared);

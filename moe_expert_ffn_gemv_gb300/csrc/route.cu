@@ -9,15 +9,14 @@
 //                         bytes of fp32); the warps' partial sums are added in
 //                         a fixed order, so the fp32 logits are reproducible
 //                         run to run.
-//   topk_gate_kernel      one warp per token; each lane holds up to 8 of the
-//                         N <= 256 logits; k rounds of a warp arg-max over
-//                         (logit desc, id asc) with xor shuffles pick the
-//                         experts in output order; lane j keeps the j-th
-//                         selected logit for the gate.
+//   topk_gate_kernel      one warp per token (topk_gate_warp, route_plan.cuh).
+//   route_plan_kernel     both of the above and the union plan in one launch
+//                         (the last CTA to finish its scores does the rest).
 #include <math.h>
 
 #include "kernels.h"
 #include "moe_common.cuh"
+#include "route_plan.cuh"
 
 namespace moe {
 
@@ -48,10 +47,9 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
 constexpr int ROUTER_MAX_WARPS = 16;
 
 template <typename T>
-__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) router_scores_kernel(const T *__restrict__ wg,
-                                                             const T *__restrict__ h, int n, int d,
-                                                             int n_experts,
-                                                             float *__restrict__ logits) {
+__device__ __forceinline__ void router_scores_cta(const T *__restrict__ wg,
+                                                  const T *__restrict__ h, int n, int d,
+                                                  int n_experts, float *__restrict__ logits) {
   __shared__ float part[ROUTER_MAX_WARPS][TOKENS_PER_CTA];
   const int e = blockIdx.x;
   const int t0 = blockIdx.y * TOKENS_PER_CTA;
@@ -90,83 +88,64 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) router_scores_kernel(co
   }
 }
 
-// (v, id) beats (bv, bid): larger logit, or equal logit and lower id.
-__device__ __forceinline__ bool beats(float v, int id, float bv, int bid) {
-  return v > bv || (v == bv && id < bid);
+template <typename T>
+__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) router_scores_kernel(const T *__restrict__ wg,
+                                                             const T *__restrict__ h, int n, int d,
+                                                             int n_experts,
+                                                             float *__restrict__ logits) {
+  router_scores_cta(wg, h, n, d, n_experts, logits);
 }
-
-constexpr int MAX_PER_LANE = 8;  // N <= 256
 
 __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict__ logits, int n,
                                                         int n_experts, int k, int gate,
                                                         int32_t *__restrict__ ids,
                                                         float *__restrict__ w) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= n) return;
-  const float *z = logits + int64_t(t) * n_experts;
-  float v[MAX_PER_LANE];
-  bool taken[MAX_PER_LANE];
-#pragma unroll
-  for (int i = 0; i < MAX_PER_LANE; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < n_experts ? z[e] : -INFINITY;
-    taken[i] = e >= n_experts;
+  topk_gate_warp(logits + int64_t(t) * n_experts, n_experts, k, gate, ids + int64_t(t) * k,
+                 w + int64_t(t) * k);
+}
+
+// Router scores, top-k + gate and the union plan in one launch.  Every CTA
+// computes its (expert, 8-token) scores as router_scores_kernel does, then
+// takes a ticket; the CTA that takes the last ticket (so all scores are
+// written) runs the top-k of every token (one warp per token) and then
+// union_plan_block, and resets the ticket counter for the next call.
+template <typename T>
+__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) route_plan_kernel(
+    const T *__restrict__ wg, const T *__restrict__ h, int n, int d, int n_experts, int k,
+    int gate, int n_shared, int64_t expert_bytes, float *logits, int32_t *ids, float *w,
+    int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
+    int64_t *union_bytes, int32_t *err, unsigned int *counter) {
+  router_scores_cta(wg, h, n, d, n_experts, logits);
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's scores before its ticket
+    const unsigned int ticket = atomicAdd(counter, 1u);
+    s_last = ticket == gridDim.x * gridDim.y - 1;
   }
-  float my_sel = -INFINITY;  // lane j < k: logit of the j-th selected expert
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < MAX_PER_LANE; ++i)
-      if (!taken[i] && beats(v[i], lane + 32 * i, bv, bid)) {
-        bv = v[i];
-        bid = lane + 32 * i;
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (beats(ov, oid, bv, bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) {
-#pragma unroll
-      for (int i = 0; i < MAX_PER_LANE; ++i)
-        if (i == (bid >> 5)) taken[i] = true;
-    }
-    if (lane == j) my_sel = bv;
-    if (lane == 0) ids[int64_t(t) * k + j] = bid;
-  }
-  // gate weights
-  const bool mine = lane < k;
-  float num = 0.f, den = 0.f;
-  if (gate == MOE_GATE_SOFTMAX) {
-    float zmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < MAX_PER_LANE; ++i)
-      if (lane + 32 * i < n_experts) zmax = fmaxf(zmax, v[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < MAX_PER_LANE; ++i)
-      if (lane + 32 * i < n_experts) s += expf(v[i] - zmax);
-    den = s;
-    num = mine ? expf(my_sel - zmax) : 0.f;
-  } else if (gate == MOE_GATE_SOFTMAX_RENORM) {
-    const float zmax = __shfl_sync(0xffffffffu, my_sel, 0);  // the largest selected
-    num = mine ? expf(my_sel - zmax) : 0.f;
-    den = num;
-  } else {
-    num = mine ? 1.f / (1.f + expf(-my_sel)) : 0.f;
-    den = num;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (mine) w[int64_t(t) * k + lane] = num / den;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  for (int t = warp; t < n; t += n_warps)
+    topk_gate_warp(logits + int64_t(t) * n_experts, n_experts, k, gate, ids + int64_t(t) * k,
+                   w + int64_t(t) * k);
+  __syncthreads();  // ids of all tokens visible to the whole CTA
+  __shared__ PlanSmem S;
+  union_plan_block(S, ids, n * k, n_experts, n_shared, expert_bytes, hist, uniq, n_uniq, offs,
+                   perm, union_bytes, err);
+  if (threadIdx.x == 0) *counter = 0u;
+}
+
+// Warps per router CTA: one per 256 columns of d, at least 8 (the fused
+// kernel's last CTA gives one thread per expert to the union plan) and at
+// most 16.  Both router kernels use the same count, so they add the same
+// partial sums in the same order and produce identical scores.
+int router_warps(int d) {
+  const int w = (d + 255) / 256;
+  return w < 8 ? 8 : w > ROUTER_MAX_WARPS ? ROUTER_MAX_WARPS : w;
 }
 
 }  // namespace
@@ -174,8 +153,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict_
 cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h, int n, int d,
                                  int n_experts, float *logits, cudaStream_t stream) {
   dim3 grid(n_experts, (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
-  int warps = (d + 255) / 256;
-  warps = warps < 1 ? 1 : warps > ROUTER_MAX_WARPS ? ROUTER_MAX_WARPS : warps;
+  const int warps = router_warps(d);
   if (bf16)
     router_scores_kernel<__nv_bfloat16><<<grid, warps * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(router_w), static_cast<const __nv_bfloat16 *>(h), n, d,
@@ -184,6 +162,26 @@ cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h,
     router_scores_kernel<float><<<grid, warps * 32, 0, stream>>>(
         static_cast<const float *>(router_w), static_cast<const float *>(h), n, d, n_experts,
         logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, int n, int d,
+                              int n_experts, int k, int gate, int n_shared, int64_t expert_bytes,
+                              float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
+                              int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
+                              int32_t *err, unsigned int *counter, cudaStream_t stream) {
+  dim3 grid(n_experts, (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
+  const int warps = router_warps(d);
+  if (bf16)
+    route_plan_kernel<__nv_bfloat16><<<grid, warps * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(router_w), static_cast<const __nv_bfloat16 *>(h), n, d,
+        n_experts, k, gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, perm,
+        union_bytes, err, counter);
+  else
+    route_plan_kernel<float><<<grid, warps * 32, 0, stream>>>(
+        static_cast<const float *>(router_w), static_cast<const float *>(h), n, d, n_experts, k,
+        gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, perm, union_bytes,
+        err, counter);
   return cudaGetLastError();
 }
 

@@ -102,3 +102,49 @@ def test_plan_flags_out_of_range_ids(mv):
     assert err == 7  # MOE_ERR_DEVICE_INPUT
     valid = ids[(ids >= 0) & (ids < 64)]
     assert U == len(set(valid.tolist())) and hist.sum() == valid.size
+
+
+ROUTE_PLAN_CASES = [(synth.TINY, 4), (synth.OLMOE, 8), (synth.QWEN3, 61), (synth.GPTOSS, 16),
+                    (synth.DSV3, 8), (synth.DSV3, 64), (synth.DSV3, 1)]
+
+
+@pytest.mark.parametrize("cfg,n", ROUTE_PLAN_CASES, ids=lambda x: getattr(x, "name", str(x)))
+def test_fused_route_plan_equals_separate_calls(mv, cfg, n):
+    # one launch (scores, top-k, gate, plan) == moe_route_topk then moe_union_plan, bit for bit,
+    # on three calls in a row (the ticket counter must reset itself)
+    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 32)
+    layer = synth.make_layer(small, seed=31).to("cuda")
+    vl = mv.VerifyLayer(layer, 64)
+    for rep in range(3):
+        h = synth.make_hidden(small, n, seed=40 + rep).cuda()
+        vl.route(h, n)
+        vl.union_plan(n)
+        torch.cuda.synchronize()
+        ref = [t.clone() for t in (vl.ids, vl.w, vl.logits, vl.plan.hist, vl.plan.uniq,
+                                   vl.plan.n_uniq, vl.plan.offs, vl.plan.perm,
+                                   vl.plan.union_bytes)]
+        for t in (vl.ids, vl.plan.perm, vl.plan.uniq):
+            t.fill_(-3)
+        vl.route_plan(h, n)
+        torch.cuda.synchronize()
+        U = int(vl.plan.n_uniq[0])
+        k = small.top_k
+        got = [vl.ids[:n * k], vl.w[:n * k], vl.logits[:n * small.n_experts], vl.plan.hist,
+               vl.plan.uniq[:U], vl.plan.n_uniq[:1], vl.plan.offs[:U + 1], vl.plan.perm[:n * k],
+               vl.plan.union_bytes[:1]]
+        want = [ref[0][:n * k], ref[1][:n * k], ref[2][:n * small.n_experts], ref[3], ref[4][:U],
+                ref[5][:1], ref[6][:U + 1], ref[7][:n * k], ref[8][:1]]
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+        assert vl.last_error() == 0
+        # the ticket counter in the workspace header is back at zero
+        assert int(vl.workspace[64:68].view(torch.int32)[0]) == 0
+
+
+def test_fused_route_plan_empty(mv):
+    layer = synth.make_layer(synth.shrink(synth.OLMOE, 2048, 32), seed=3).to("cuda")
+    vl = mv.VerifyLayer(layer, 8)
+    vl.plan.n_uniq.fill_(5)
+    vl.route_plan(torch.empty(0, 2048, dtype=torch.bfloat16, device="cuda"), 0)
+    torch.cuda.synchronize()
+    assert int(vl.plan.n_uniq[0]) == 0 and int(vl.plan.offs[0]) == 0
