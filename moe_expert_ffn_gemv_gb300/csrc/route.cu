@@ -24,32 +24,45 @@ namespace {
 
 constexpr int TOKENS_PER_CTA = 8;
 
-__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
-  const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
-  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
 // One CTA per (expert, group of 8 tokens), one warp per 256-column chunk of
-// d (up to 16 warps; larger d loops), so a lane issues its loads together and
+// d (8 to 16 warps; larger d loops), so a lane issues its loads together and
 // the whole dot product costs one or two L2 round trips.
 constexpr int ROUTER_MAX_WARPS = 16;
+
+// 8 consecutive elements kept as loaded (bf16: one 16-byte word; fp32: two)
+// and widened to fp32 only at use, so a thread can hold its 8 tokens' pieces
+// in few registers and two CTAs fit on an SM.
+struct Raw8Bf16 {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+    v = __ldg(reinterpret_cast<const uint4 *>(p));
+  }
+  __device__ __forceinline__ float at(int i) const {
+    const uint32_t w = i < 2 ? v.x : i < 4 ? v.y : i < 6 ? v.z : v.w;
+    return (i & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+  }
+};
+struct Raw8F32 {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float *p) {
+    a = __ldg(reinterpret_cast<const float4 *>(p));
+    b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  }
+  __device__ __forceinline__ float at(int i) const {
+    const float4 &q = i < 4 ? a : b;
+    const int j = i & 3;
+    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+  }
+};
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> { using type = Raw8Bf16; };
+template <> struct Raw8<float> { using type = Raw8F32; };
 
 template <typename T>
 __device__ __forceinline__ void router_scores_cta(const T *__restrict__ wg,
                                                   const T *__restrict__ h, int n, int d,
                                                   int n_experts, float *__restrict__ logits) {
+  using R = typename Raw8<T>::type;
   __shared__ float part[ROUTER_MAX_WARPS][TOKENS_PER_CTA];
   const int e = blockIdx.x;
   const int t0 = blockIdx.y * TOKENS_PER_CTA;
@@ -59,18 +72,19 @@ __device__ __forceinline__ void router_scores_cta(const T *__restrict__ wg,
   float acc[TOKENS_PER_CTA];
 #pragma unroll
   for (int t = 0; t < TOKENS_PER_CTA; ++t) acc[t] = 0.f;
+#pragma unroll 2
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
-    float wv[8];
-    load8(wg + int64_t(e) * d + c, wv);
-    float hv[TOKENS_PER_CTA][8];
+    R wv;
+    wv.load(wg + int64_t(e) * d + c);
+    R hv[TOKENS_PER_CTA];
 #pragma unroll
     for (int t = 0; t < TOKENS_PER_CTA; ++t)
-      if (t < nt) load8(h + int64_t(t0 + t) * d + c, hv[t]);
+      if (t < nt) hv[t].load(h + int64_t(t0 + t) * d + c);
 #pragma unroll
     for (int t = 0; t < TOKENS_PER_CTA; ++t)
       if (t < nt) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[t] = fmaf(wv[i], hv[t][i], acc[t]);
+        for (int i = 0; i < 8; ++i) acc[t] = fmaf(wv.at(i), hv[t].at(i), acc[t]);
       }
   }
 #pragma unroll
@@ -89,7 +103,7 @@ __device__ __forceinline__ void router_scores_cta(const T *__restrict__ wg,
 }
 
 template <typename T>
-__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) router_scores_kernel(const T *__restrict__ wg,
+__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) router_scores_kernel(const T *__restrict__ wg,
                                                              const T *__restrict__ h, int n, int d,
                                                              int n_experts,
                                                              float *__restrict__ logits) {
@@ -112,7 +126,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict_
 // written) runs the top-k of every token (one warp per token) and then
 // union_plan_block, and resets the ticket counter for the next call.
 template <typename T>
-__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32) route_plan_kernel(
+__global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
     const T *__restrict__ wg, const T *__restrict__ h, int n, int d, int n_experts, int k,
     int gate, int n_shared, int64_t expert_bytes, float *logits, int32_t *ids, float *w,
     int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
