@@ -57,6 +57,11 @@ def parse():
     p.add_argument("--no-sweep", action="store_true", help="skip the n = 1..64 engine sweep")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     p.add_argument("--sweep-max", type=int, default=64)
+    p.add_argument("--sweep-min", type=int, default=1)
+    p.add_argument("--sweep-config", default=None, choices=sorted(synth.CONFIGS),
+                   help="run only the dedup-vs-per-slot sweep on this layer shape")
+    p.add_argument("--rho", type=float, default=None, help="chain/tree correlation for the sweep")
+    p.add_argument("--sigma", type=float, default=None, help="tree noise for the sweep")
     p.add_argument("--experts", type=int, default=None,
                    help="routed experts of the layer (default 256); fewer make a small profiling case")
     return p.parse_args()
@@ -340,21 +345,22 @@ def flush_l2(buf_a, buf_b):
     buf_b.sum()               # ... then read more than L2, so no dirty lines remain
 
 
-def engine_sweep(mv, layer, h_all, n_max, eb, reps=5):
+def engine_sweep(mv, layer, h_all, n_max, eb, reps=5, n_min=1, cfg=None):
     """µs per pass of each engine's expert call (after routing and planning,
-    which are shared) for n = 1..n_max, L2 flushed before each timed call."""
+    which are shared) for n = n_min..n_max, L2 flushed before each timed call;
+    u_bar, r and the crossover as "Expert Bytes, Kernel Bandwidth and the Best
+    Draft Length" defines them (moe_expert_ffn_gemv_gb300/crossover.py)."""
+    from moe_expert_ffn_gemv_gb300 import crossover as X
+    cfg = cfg or CFG
     vl = mv.VerifyLayer(layer, 64)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     a = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
     b = torch.ones_like(a)
     stream = torch.cuda.current_stream()
-    rows = []
-    crossover = None
-    k1 = CFG.top_k + CFG.n_shared
-    for n in range(1, n_max + 1):
+    raw = []
+    for n in range(n_min, n_max + 1):
         h = h_all[:n].contiguous()
-        vl.route(h, n)
-        vl.union_plan(n)
+        vl.route_plan(h, n)
         vl.dedup(h, n)
         vl.perslot(h, n)
         torch.cuda.synchronize()
@@ -370,20 +376,36 @@ def engine_sweep(mv, layer, h_all, n_max, eb, reps=5):
                 (vl.dedup if eng == "dedup" else vl.perslot)(h, n)
                 e1.record(stream)
                 torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1) * 1e3)
+                ts.append(e0.elapsed_time(e1) * 1e-3)
             t[eng] = statistics.median(ts)
         assert vl.last_error() == 0
-        ub = (U + CFG.n_shared) * eb
-        rb = n * k1 * eb
-        u_bar = ub / rb
-        r = (ub / t["dedup"]) / (rb / t["perslot"])
-        rows.append([n, U, round(t["dedup"], 1), round(t["perslot"], 1), round(u_bar, 3),
-                     round(r, 3), round(ub / t["dedup"] / 1e3, 1)])
-        if crossover is None and t["dedup"] < t["perslot"]:
-            crossover = n
-    return {"columns": ["n", "U", "us_dedup", "us_perslot", "u_bar", "r", "gbs_dedup_union"],
-            "rows": rows, "crossover_n": crossover,
+        raw.append(dict(n=n, U=U, t_dedup=t["dedup"], t_slot=t["perslot"]))
+    an = X.analyse(raw, cfg.top_k, eb, cfg.n_shared)
+    rows = [[a_["n"], a_["U"], round(1e6 * a_["t_dedup"], 1), round(1e6 * a_["t_slot"], 1),
+             round(a_["u_bar"], 3), round(a_["r"], 3), round(a_["beta_dedup"] / 1e9, 1),
+             round(a_["beta_slot"] / 1e9, 1)] for a_ in an]
+    return {"columns": ["n", "U", "us_dedup", "us_perslot", "u_bar", "r", "gbs_dedup_union",
+                        "gbs_perslot_requested"],
+            "rows": rows,
+            "crossover_n": X.crossover([a_["n"] for a_ in an], [a_["t_dedup"] for a_ in an],
+                                       [a_["t_slot"] for a_ in an]),
+            "criterion_agrees": all(a_["criterion_dedup_faster"] == a_["measured_dedup_faster"]
+                                    for a_ in an),
             "l2": "flushed (2x L2 written then 2x L2 read) before each timed call"}
+
+
+def run_sweep_only(args):
+    """--sweep-config NAME: the engine sweep alone on another layer shape."""
+    from moe_expert_ffn_gemv_gb300 import binding as mv
+    torch.cuda.set_device(0)
+    cfg = synth.CONFIGS[args.sweep_config]
+    layer = synth.make_layer(cfg, seed=1, device="cuda")
+    h_all = synth.make_hidden(cfg, 64, seed=3, device="cuda", rho=args.rho, sigma=args.sigma)
+    eb = sum(mv.moe_expert_bytes(mv.make_desc(cfg, 64)))
+    sw = engine_sweep(mv, layer, h_all, args.sweep_max, eb, n_min=args.sweep_min, cfg=cfg)
+    print(json.dumps({"sweep_config": cfg.name, "rho": args.rho if args.rho is not None else cfg.rho,
+                      "sigma": args.sigma if args.sigma is not None else cfg.sigma,
+                      "hidden": cfg.hidden, **sw}))
 
 
 # ------------------------------------------------------------- cpu / oracle
@@ -468,7 +490,9 @@ def main():
         from dataclasses import replace
         CFG = replace(CFG, n_experts=args.experts)
         WORKLOAD += f" ({args.experts} routed experts: profiling case)"
-    if args.impl == "reference":
+    if args.sweep_config:
+        run_sweep_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
