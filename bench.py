@@ -60,6 +60,9 @@ def parse():
     p.add_argument("--sweep-min", type=int, default=1)
     p.add_argument("--sweep-config", default=None, choices=sorted(synth.CONFIGS),
                    help="run only the dedup-vs-per-slot sweep on this layer shape")
+    p.add_argument("--fit-config", default=None, choices=sorted(synth.CONFIGS),
+                   help="fit the bandwidth cost model on this layer shape and test it")
+    p.add_argument("--windows", type=int, default=4, help="routing windows to fit (and to test)")
     p.add_argument("--rho", type=float, default=None, help="chain/tree correlation for the sweep")
     p.add_argument("--sigma", type=float, default=None, help="tree noise for the sweep")
     p.add_argument("--experts", type=int, default=None,
@@ -394,6 +397,82 @@ def engine_sweep(mv, layer, h_all, n_max, eb, reps=5, n_min=1, cfg=None):
             "l2": "flushed (2x L2 written then 2x L2 read) before each timed call"}
 
 
+def run_fit(args):
+    """--fit-config NAME: fit each engine's effective bandwidth per n on
+    --windows routing windows, predict time and saving on as many held-out
+    windows, and check the saving bound and the faster-kernel criterion."""
+    from moe_expert_ffn_gemv_gb300 import binding as mv
+    from moe_expert_ffn_gemv_gb300 import crossover as X
+    torch.cuda.set_device(0)
+    cfg = synth.CONFIGS[args.fit_config]
+    layer = synth.make_layer(cfg, seed=1, device="cuda")
+    eb = sum(mv.moe_expert_bytes(mv.make_desc(cfg, 64)))
+    vl = mv.VerifyLayer(layer, 64)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    fa = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    fb = torch.ones_like(fa)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps=3):
+        ts = []
+        for _ in range(reps):
+            flush_l2(fa, fb)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    fit_w, test_w = [], []
+    for w in range(2 * args.windows):
+        h_all = synth.make_hidden(cfg, 64, seed=1000 + w, device="cuda", rho=args.rho,
+                                  sigma=args.sigma)
+        for n in range(1, args.sweep_max + 1):
+            h = h_all[:n].contiguous()
+            vl.route_plan(h, n)
+            vl.dedup(h, n)
+            vl.perslot(h, n)
+            torch.cuda.synchronize()
+            U = int(vl.plan.n_uniq[0])
+            row = dict(n=n, U=U, t_dedup=timed(lambda: vl.dedup(h, n)),
+                       t_slot=timed(lambda: vl.perslot(h, n)))
+            (fit_w if w < args.windows else test_w).append(row)
+    assert vl.last_error() == 0
+    k, sh = cfg.top_k, cfg.n_shared
+    model = X.fit_bandwidths(fit_w, k, eb, sh)
+    ev = X.evaluate(model, test_w, k, eb, sh)
+    ns = sorted(model)
+    med = lambda xs: statistics.median(xs) if xs else float("nan")
+    s_meas = {n: med([e["saving"] for e in ev if e["n"] == n]) for n in ns}
+    s_pred = {n: med([e["saving_hat"] for e in ev if e["n"] == n]) for n in ns}
+    cross_meas = next((n for n in ns if s_meas[n] > 0), None)
+    cross_pred = next((n for n in ns if s_pred[n] > 0), None)
+    # (19): where the criterion is certain for the fit's eps, it must pick the faster kernel
+    certain = agree = 0
+    for e, w in zip(ev, test_w):
+        m = model[w["n"]]
+        ub = X.u_bar(w["U"], w["n"], k, sh)
+        r_hat = m["beta_dedup"] / m["beta_slot"]
+        if X.faster_kernel_is_certain(r_hat, ub, m["eps"]):
+            certain += 1
+            agree += (ub < r_hat) == (w["t_dedup"] < w["t_slot"])
+    print(json.dumps({
+        "fit_config": cfg.name, "windows_fit": args.windows, "windows_test": args.windows,
+        "n_max": args.sweep_max,
+        "model": {str(n): {"gbs_slot": round(model[n]["beta_slot"] / 1e9, 1),
+                           "gbs_dedup": round(model[n]["beta_dedup"] / 1e9, 1),
+                           "eps": round(model[n]["eps"], 4)} for n in ns},
+        "saving_us": {str(n): [round(1e6 * s_meas[n], 2), round(1e6 * s_pred[n], 2)] for n in ns},
+        "max_saving_error_us": round(1e6 * max(abs(e["saving"] - e["saving_hat"]) for e in ev), 2),
+        "inside_bound_18": f"{sum(e['inside'] for e in ev)} of {len(ev)}",
+        "sign_of_saving_predicted": f"{sum(e['sign_ok'] for e in ev)} of {len(ev)}",
+        "criterion_19_certain_and_right": f"{agree} of {certain}",
+        "crossover_measured": cross_meas, "crossover_predicted": cross_pred}))
+
+
 def run_sweep_only(args):
     """--sweep-config NAME: the engine sweep alone on another layer shape."""
     from moe_expert_ffn_gemv_gb300 import binding as mv
@@ -490,7 +569,9 @@ def main():
         from dataclasses import replace
         CFG = replace(CFG, n_experts=args.experts)
         WORKLOAD += f" ({args.experts} routed experts: profiling case)"
-    if args.sweep_config:
+    if args.fit_config:
+        run_fit(args)
+    elif args.sweep_config:
         run_sweep_only(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -15,6 +15,7 @@ union member (U + 1).
 """
 from __future__ import annotations
 
+import math
 from typing import Dict, Iterable, List, Optional, Sequence
 
 
@@ -67,4 +68,78 @@ def analyse(rows: Iterable[Dict], k: int, expert_bytes: int, n_shared: int = 0) 
         out.append(dict(row, u_bar=uu, beta_dedup=bd, beta_slot=bs, r=r,
                         criterion_dedup_faster=dedup_faster(uu, r),
                         measured_dedup_faster=row["t_dedup"] < row["t_slot"]))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Bandwidth-fit cost model ("Expert Bytes, Kernel Bandwidth and the Best Draft
+# Length", abstract, Fig. 2, Tables 1-3): each kernel's time on one layer's
+# expert operation is its requested bytes over an effective bandwidth that
+# already includes the operation's fixed work (Table 1 note).  The bandwidths
+# are fitted per pass size n on one set of routing windows (median over the
+# windows, as Fig. 2 plots); the bytes of other windows over those bandwidths
+# predict each kernel's time and the saving of deduplication.  The error
+# bounds of Table 2 are checked for a relative bandwidth error eps.
+
+def fit_bandwidths(windows: Iterable[Dict], k: int, expert_bytes: int, n_shared: int = 0) -> Dict:
+    """windows: dicts with n, U, t_dedup, t_slot (seconds).  Returns, per n,
+    beta_slot and beta_dedup (median over the windows of bytes / time) and
+    eps: the largest relative deviation of a window's bandwidth from the fit."""
+    import statistics
+    by_n: Dict[int, List[Dict]] = {}
+    for w in windows:
+        by_n.setdefault(w["n"], []).append(w)
+    model = {}
+    for n, ws in sorted(by_n.items()):
+        bs = [requested_bytes_perslot(n, k, expert_bytes, n_shared) / w["t_slot"] for w in ws]
+        bd = [union_bytes(w["U"], expert_bytes, n_shared) / w["t_dedup"] for w in ws]
+        b_slot, b_dedup = statistics.median(bs), statistics.median(bd)
+        eps = max([abs(x / b_slot - 1) for x in bs] + [abs(x / b_dedup - 1) for x in bd])
+        model[n] = dict(beta_slot=b_slot, beta_dedup=b_dedup, eps=eps)
+    return model
+
+
+def predict(model: Dict, n: int, U: int, k: int, expert_bytes: int, n_shared: int = 0) -> Dict:
+    """Predicted time of each kernel (its memory term M = bytes / bandwidth)
+    and predicted saving S = tau_slot - tau_dedup for one pass of n tokens with
+    union size U."""
+    m = model[n]
+    m_slot = requested_bytes_perslot(n, k, expert_bytes, n_shared) / m["beta_slot"]
+    m_dedup = union_bytes(U, expert_bytes, n_shared) / m["beta_dedup"]
+    return dict(tau_slot=m_slot, tau_dedup=m_dedup, saving=m_slot - m_dedup)
+
+
+def bound_verify_time(M: float, eps: float) -> float:
+    """Table 2, (17): |tau_hat - tau| <= eps/(1-eps) * M."""
+    return eps / (1.0 - eps) * M
+
+
+def bound_saving(M_slot: float, M_dedup: float, eps: float) -> float:
+    """Table 2, (18): |S_hat - S| <= eps/(1-eps) * (M_slot + M_dedup)."""
+    return eps / (1.0 - eps) * (M_slot + M_dedup)
+
+
+def faster_kernel_is_certain(r: float, ubar: float, eps: float) -> bool:
+    """Table 2, (19): the two sides of u_bar < r cannot swap under relative
+    bandwidth errors up to eps when |ln r - ln u_bar| > ln((1+eps)/(1-eps))."""
+    return abs(math.log(r) - math.log(ubar)) > math.log((1.0 + eps) / (1.0 - eps))
+
+
+def evaluate(model: Dict, windows: Iterable[Dict], k: int, expert_bytes: int,
+             n_shared: int = 0) -> List[Dict]:
+    """Held-out windows against the fitted model: predicted and measured
+    saving, the saving bound (18) for the fit's eps, whether the measured
+    saving lies inside it, and whether the faster kernel was predicted."""
+    out = []
+    for w in windows:
+        n, U = w["n"], w["U"]
+        if n not in model:
+            continue
+        pr = predict(model, n, U, k, expert_bytes, n_shared)
+        eps = model[n]["eps"]
+        S = w["t_slot"] - w["t_dedup"]
+        bnd = bound_saving(pr["tau_slot"], pr["tau_dedup"], eps) if eps < 1 else math.inf
+        out.append(dict(n=n, U=U, saving=S, saving_hat=pr["saving"], bound=bnd,
+                        inside=abs(pr["saving"] - S) <= bnd,
+                        sign_ok=(pr["saving"] > 0) == (S > 0)))
     return out

@@ -48,3 +48,64 @@ def test_u_bar_bounds_and_shared_expert():
     assert X.u_bar(39, 8, 8, n_shared=1) == 40 / 72
     assert X.crossover([1, 2, 3], [5, 4, 2], [5, 4.5, 3]) == 2
     assert X.crossover([1, 2], [5, 6], [4, 5]) is None
+
+
+# ------------------------------------------------ cost model and Table 2 bounds
+import math
+
+import numpy as np
+
+
+def test_bound_17_holds_for_any_bandwidth_error_within_eps():
+    # tau = B / beta; an estimate beta_hat = beta (1 + e), |e| <= eps, predicts
+    # tau_hat = B / beta_hat: |tau_hat - tau| <= eps/(1-eps) * tau
+    rng = np.random.default_rng(1)
+    for _ in range(2000):
+        B = rng.uniform(1e6, 1e10)
+        beta = rng.uniform(1e10, 1e13)
+        eps = rng.uniform(0.0, 0.5)
+        e = rng.uniform(-eps, eps)
+        tau, tau_hat = B / beta, B / (beta * (1 + e))
+        assert abs(tau_hat - tau) <= X.bound_verify_time(tau, eps) * (1 + 1e-12)
+    # and the bound is reached at e = -eps
+    B, beta, eps = 1e9, 5e12, 0.1
+    tau, tau_hat = B / beta, B / (beta * (1 - eps))
+    assert math.isclose(abs(tau_hat - tau), X.bound_verify_time(tau, eps), rel_tol=1e-12)
+
+
+def test_bound_18_and_19_hold_for_any_bandwidth_errors_within_eps():
+    rng = np.random.default_rng(2)
+    for _ in range(2000):
+        Bs, Bd = rng.uniform(1e8, 1e10, size=2)
+        bs, bd = rng.uniform(1e11, 1e13, size=2)
+        eps = rng.uniform(0.0, 0.4)
+        es, ed = rng.uniform(-eps, eps, size=2)
+        S = Bs / bs - Bd / bd
+        S_hat = Bs / (bs * (1 + es)) - Bd / (bd * (1 + ed))
+        assert abs(S_hat - S) <= X.bound_saving(Bs / bs, Bd / bd, eps) * (1 + 1e-12)
+        # (19): r = bd/bs, u_bar = Bd/Bs; dedup faster <=> u_bar < r
+        r, ub = bd / bs, Bd / Bs
+        r_hat = bd * (1 + ed) / (bs * (1 + es))
+        if X.faster_kernel_is_certain(r, ub, eps):
+            assert (ub < r) == (ub < r_hat)
+
+
+def test_fit_predict_evaluate_recovers_a_known_model():
+    # windows generated from exact bandwidths: the fit recovers them, eps is 0,
+    # predictions are exact and every point lies inside the (zero) bound
+    k, b, sh = 8, 44_050_944, 1
+    bslot = {2: 5.0e12, 8: 6.0e12}
+    bded = {2: 4.5e12, 8: 5.8e12}
+    wins = []
+    for n in (2, 8):
+        for U in (n * 3, n * 4, n * 5):
+            wins.append(dict(n=n, U=U, t_slot=X.requested_bytes_perslot(n, k, b, sh) / bslot[n],
+                             t_dedup=X.union_bytes(U, b, sh) / bded[n]))
+    model = X.fit_bandwidths(wins, k, b, sh)
+    for n in (2, 8):
+        assert math.isclose(model[n]["beta_slot"], bslot[n], rel_tol=1e-12)
+        assert math.isclose(model[n]["beta_dedup"], bded[n], rel_tol=1e-12)
+        assert model[n]["eps"] < 1e-12
+    ev = X.evaluate(model, wins, k, b, sh)
+    assert all(e["inside"] and e["sign_ok"] for e in ev)
+    assert all(abs(e["saving"] - e["saving_hat"]) < 1e-15 for e in ev)
