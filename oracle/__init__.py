@@ -78,6 +78,14 @@ def lib():
         L.orc_expert_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_int64)]
+        L.orc_expert_budget.restype = ctypes.c_int
+        L.orc_expert_budget.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p]
+        L.orc_budget_plan.restype = ctypes.c_int
+        L.orc_budget_plan.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      p, p, p, p, p, p, p]
+        L.orc_verify_budget.restype = ctypes.c_int
+        L.orc_verify_budget.argtypes = [ctypes.POINTER(_Layer), p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, p, p, p, p, p]
         _lib = L
     return _lib
 
@@ -219,3 +227,60 @@ def expert_bytes(d: int, inter: int, w_type: int):
     wb, sb = ctypes.c_int64(), ctypes.c_int64()
     lib().orc_expert_bytes(d, inter, w_type, ctypes.byref(wb), ctypes.byref(sb))
     return wb.value, sb.value
+
+
+def expert_budget(ids: np.ndarray, w: np.ndarray, n_experts: int, budget: int):
+    """Verification-time expert budget (MoE-Spec): (keep [N] bool, score [N]
+    f64, number kept).  score[e] sums the weights of the slots naming e in
+    ascending slot order; the kept experts are the first `budget` used ones
+    by (score descending, id ascending).  w is widened to double exactly."""
+    flat = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).ravel())
+    wf = np.ascontiguousarray(np.asarray(w).ravel(), dtype=np.float64)
+    assert flat.size == wf.size and budget >= 0
+    assert flat.size == 0 or (flat.min() >= 0 and flat.max() < n_experts)
+    keep = np.zeros(n_experts, dtype=np.uint8)
+    score = np.zeros(n_experts, dtype=np.float64)
+    kept = lib().orc_expert_budget(_ptr(flat), _ptr(wf), flat.size, n_experts, budget,
+                                   _ptr(keep), _ptr(score))
+    return keep.astype(bool), score, kept
+
+
+def budget_plan(ids: np.ndarray, w: np.ndarray, n_experts: int, budget: int):
+    """The union plan of the kept slots under an expert budget:
+    (U, hist [N], uniq [U], offs [U+1], perm [kept slots], w_kept [n*k] f64,
+    keep [N] bool)."""
+    flat = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).ravel())
+    wf = np.ascontiguousarray(np.asarray(w).ravel(), dtype=np.float64)
+    assert flat.size == wf.size and budget >= 0
+    assert flat.size == 0 or (flat.min() >= 0 and flat.max() < n_experts)
+    keep = np.zeros(n_experts, dtype=np.uint8)
+    score = np.zeros(n_experts, dtype=np.float64)
+    hist = np.zeros(n_experts, dtype=np.int32)
+    uniq = np.zeros(n_experts, dtype=np.int32)
+    offs = np.zeros(n_experts + 1, dtype=np.int32)
+    perm = np.zeros(max(flat.size, 1), dtype=np.int32)
+    w_kept = np.zeros(max(flat.size, 1), dtype=np.float64)
+    U = lib().orc_budget_plan(_ptr(flat), _ptr(wf), flat.size, n_experts, budget, _ptr(keep),
+                              _ptr(score), _ptr(hist), _ptr(uniq), _ptr(offs), _ptr(perm),
+                              _ptr(w_kept))
+    return (U, hist, uniq[:U].copy(), offs[:U + 1].copy(), perm[:offs[U]].copy(),
+            w_kept[:flat.size].copy(), keep.astype(bool))
+
+
+def verify_budget(layer: Layer, h: np.ndarray, budget: int, threads: int = 1):
+    """The pass of all n tokens under an expert budget: (ids [n][k], w [n][k]
+    f64, z [n][N] f64, y [n][d] f64, keep [N] bool).  Routing is the same as
+    verify(); each token's output sums only its slots whose expert is kept
+    (plus the shared expert), with the weights not renormalised."""
+    h = np.ascontiguousarray(h)
+    n = h.shape[0]
+    assert budget >= 0
+    ids = np.zeros((n, layer.top_k), dtype=np.int32)
+    w = np.zeros((n, layer.top_k), dtype=np.float64)
+    z = np.zeros((n, layer.n_experts), dtype=np.float64)
+    y = np.zeros((n, layer.d), dtype=np.float64)
+    keep = np.zeros(layer.n_experts, dtype=np.uint8)
+    c = layer._c()
+    lib().orc_verify_budget(ctypes.byref(c), _ptr(h), n, threads, budget, _ptr(ids), _ptr(w),
+                            _ptr(z), _ptr(y), _ptr(keep))
+    return ids, w, z, y, keep.astype(bool)

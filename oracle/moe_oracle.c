@@ -245,19 +245,34 @@ static void expert_ptrs(const orc_layer *L, int e, const void **w13,
   }
 }
 
-/* The whole layer for one token t. */
-static void verify_token(const orc_layer *L, const void *hs, int t,
-                         int32_t *ids, double *w, double *z, double *y) {
+/* Router scores, top-k and gate of token t. */
+static void route_token(const orc_layer *L, const void *hs, int t, int32_t *ids,
+                        double *w, double *z) {
   int d = L->d;
   double *h = (double *)malloc(sizeof(double) * (size_t)d);
-  double *a = (double *)malloc(sizeof(double) * (size_t)L->inter);
   for (int c = 0; c < d; ++c)
     h[c] = load_elem(hs, L->act_type, (size_t)t * d + c);
   orc_router_scores(L, h, z);
   orc_topk(z, L->n_experts, L->top_k, ids);
   orc_gate(z, L->n_experts, ids, L->top_k, L->gate, w);
+  free(h);
+}
+
+/* The layer output of token t from its routed ids and weights:
+ * y = sum over j of w[j] * FFN_{ids[j]}(h), in slot order, then the shared
+ * expert with weight 1.  With `keep` (NULL = every expert), a slot whose
+ * expert e has keep[e] == 0 is left out of the sum. */
+static void ffn_token(const orc_layer *L, const void *hs, int t,
+                      const int32_t *ids, const double *w, const uint8_t *keep,
+                      double *y) {
+  int d = L->d;
+  double *h = (double *)malloc(sizeof(double) * (size_t)d);
+  double *a = (double *)malloc(sizeof(double) * (size_t)L->inter);
+  for (int c = 0; c < d; ++c)
+    h[c] = load_elem(hs, L->act_type, (size_t)t * d + c);
   for (int r = 0; r < d; ++r) y[r] = 0.0;
   for (int j = 0; j < L->top_k; ++j) {
+    if (keep && !keep[ids[j]]) continue;
     const void *w13, *w2;
     const float *s13, *s2;
     expert_ptrs(L, ids[j], &w13, &s13, &w2, &s2);
@@ -269,6 +284,9 @@ static void verify_token(const orc_layer *L, const void *hs, int t,
   free(h);
 }
 
+/* What a worker does for each of its tokens. */
+enum { DO_ROUTE_AND_FFN = 0, DO_ROUTE = 1, DO_FFN = 2 };
+
 typedef struct {
   const orc_layer *L;
   const void *hs;
@@ -276,19 +294,49 @@ typedef struct {
   int n_tokens;
   int stride;
   int first;
+  int mode;
+  const uint8_t *keep;
   int32_t *ids;
   double *w, *z, *y;
 } worker_arg;
 
 static void *worker(void *p) {
   worker_arg *A = (worker_arg *)p;
+  const orc_layer *L = A->L;
   for (int i = A->first; i < A->n_tokens; i += A->stride) {
     int t = A->tokens ? A->tokens[i] : i;
-    verify_token(A->L, A->hs, t, A->ids + (size_t)i * A->L->top_k,
-                 A->w + (size_t)i * A->L->top_k,
-                 A->z + (size_t)i * A->L->n_experts, A->y + (size_t)i * A->L->d);
+    int32_t *ids = A->ids + (size_t)i * L->top_k;
+    double *w = A->w + (size_t)i * L->top_k;
+    if (A->mode != DO_FFN)
+      route_token(L, A->hs, t, ids, w, A->z + (size_t)i * L->n_experts);
+    if (A->mode != DO_ROUTE)
+      ffn_token(L, A->hs, t, ids, w, A->keep, A->y + (size_t)i * L->d);
   }
   return NULL;
+}
+
+/* Runs `worker` over n_tokens tokens on n_threads host threads. */
+static void run_workers(const orc_layer *L, const void *hs, const int32_t *tokens,
+                        int n_tokens, int n_threads, int mode,
+                        const uint8_t *keep, int32_t *ids, double *w,
+                        double *z, double *y) {
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > n_tokens) n_threads = n_tokens > 0 ? n_tokens : 1;
+  if (n_threads == 1) {
+    worker_arg A = {L, hs, tokens, n_tokens, 1, 0, mode, keep, ids, w, z, y};
+    worker(&A);
+    return;
+  }
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+  worker_arg *A = (worker_arg *)malloc(sizeof(worker_arg) * (size_t)n_threads);
+  for (int i = 0; i < n_threads; ++i) {
+    worker_arg a = {L, hs, tokens, n_tokens, n_threads, i, mode, keep, ids, w, z, y};
+    A[i] = a;
+    pthread_create(&th[i], NULL, worker, &A[i]);
+  }
+  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  free(A);
+  free(th);
 }
 
 /* The verification pass for the tokens listed in `tokens` (all n tokens in
@@ -298,23 +346,8 @@ static void *worker(void *p) {
 int orc_verify(const orc_layer *L, const void *hs, const int32_t *tokens,
                int n_tokens, int n_threads, int32_t *ids, double *w, double *z,
                double *y) {
-  if (n_threads < 1) n_threads = 1;
-  if (n_threads > n_tokens) n_threads = n_tokens > 0 ? n_tokens : 1;
-  if (n_threads == 1) {
-    worker_arg A = {L, hs, tokens, n_tokens, 1, 0, ids, w, z, y};
-    worker(&A);
-    return 0;
-  }
-  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
-  worker_arg *A = (worker_arg *)malloc(sizeof(worker_arg) * (size_t)n_threads);
-  for (int i = 0; i < n_threads; ++i) {
-    worker_arg a = {L, hs, tokens, n_tokens, n_threads, i, ids, w, z, y};
-    A[i] = a;
-    pthread_create(&th[i], NULL, worker, &A[i]);
-  }
-  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
-  free(A);
-  free(th);
+  run_workers(L, hs, tokens, n_tokens, n_threads, DO_ROUTE_AND_FFN, NULL, ids,
+              w, z, y);
   return 0;
 }
 
@@ -371,4 +404,108 @@ void orc_expert_bytes(int d, int inter, int w_type, int64_t *weights,
   if (w_type == ORC_E4M3)
     *scales = (int64_t)4 * (((int64_t)2 * inter / ORC_BLOCK) * (d / ORC_BLOCK) +
                             ((int64_t)d / ORC_BLOCK) * (inter / ORC_BLOCK));
+}
+
+/* ---------------------------------------------------------- expert budget */
+
+/* Verification-time expert budgeting, MoE-Spec: a fixed cap on the experts
+ * loaded per layer, keeping those that contribute most to verification and
+ * dropping the long tail of rarely used ones (its abstract, in the list of
+ * related papers on "Speculative Decoding for Mixture-of-Experts Models:
+ * Expert Bytes, Kernel Bandwidth and the Best Draft Length"; "The Limits of
+ * Speculation", Sec. 2.4: the per-layer expert budget is capped; "Making
+ * Every Verified Token Count", Sec. 5: the active expert set is truncated,
+ * so the output is lossy).
+ * The pages give no formula; the readings taken here:
+ *   contribution of expert e  = the sum of the gate weights of the slots
+ *                               that name e, added in ascending slot order
+ *                               in double;
+ *   kept experts              = the first `budget` of the used experts in
+ *                               the order (contribution descending, id
+ *                               ascending), all of them when U <= budget;
+ *   a dropped slot            = its term is left out of the layer output;
+ *                               the other weights are not renormalised;
+ *   the shared expert         = always applied, not counted in the budget.
+ *   keep[e]   1 for a kept expert, else 0
+ *   score[e]  the contribution (0 for an expert no slot names)
+ * Returns the number of kept experts. */
+typedef struct {
+  double score;
+  int id;
+} scored_expert;
+
+static int cmp_contribution(const void *a, const void *b) {
+  const scored_expert *x = (const scored_expert *)a, *y = (const scored_expert *)b;
+  if (x->score != y->score) return x->score < y->score ? 1 : -1;
+  return x->id < y->id ? -1 : (x->id > y->id ? 1 : 0);
+}
+
+int orc_expert_budget(const int32_t *ids, const double *w, int n_slots,
+                      int n_experts, int budget, uint8_t *keep, double *score) {
+  int *used = (int *)calloc((size_t)n_experts, sizeof(int));
+  for (int e = 0; e < n_experts; ++e) {
+    score[e] = 0.0;
+    keep[e] = 0;
+  }
+  for (int p = 0; p < n_slots; ++p) {
+    score[ids[p]] += w[p];
+    used[ids[p]] = 1;
+  }
+  scored_expert *order = (scored_expert *)malloc(sizeof(scored_expert) * (size_t)(n_experts + 1));
+  int U = 0;
+  for (int e = 0; e < n_experts; ++e)
+    if (used[e]) {
+      order[U].score = score[e];
+      order[U].id = e;
+      ++U;
+    }
+  qsort(order, (size_t)U, sizeof(scored_expert), cmp_contribution);
+  int kept = U < budget ? U : budget;
+  for (int r = 0; r < kept; ++r) keep[order[r].id] = 1;
+  free(order);
+  free(used);
+  return kept;
+}
+
+/* The union plan of the kept slots only (same layout as orc_union_plan, the
+ * dropped slots absent from hist, uniq, offs and perm), and the weights the
+ * layer output uses: w_kept[p] = w[p] for a kept slot, 0 for a dropped one.
+ * Returns the kept union size. */
+int orc_budget_plan(const int32_t *ids, const double *w, int n_slots,
+                    int n_experts, int budget, uint8_t *keep, double *score,
+                    int32_t *hist, int32_t *uniq, int32_t *offs, int32_t *perm,
+                    double *w_kept) {
+  orc_expert_budget(ids, w, n_slots, n_experts, budget, keep, score);
+  int U = 0;
+  for (int e = 0; e < n_experts; ++e) hist[e] = 0;
+  for (int p = 0; p < n_slots; ++p) {
+    w_kept[p] = keep[ids[p]] ? w[p] : 0.0;
+    if (keep[ids[p]]) hist[ids[p]] += 1;
+  }
+  for (int e = 0; e < n_experts; ++e)
+    if (hist[e] > 0) uniq[U++] = e;
+  int pos = 0;
+  for (int u = 0; u < U; ++u) {
+    offs[u] = pos;
+    for (int p = 0; p < n_slots; ++p)
+      if (uniq[u] == ids[p]) perm[pos++] = p; /* kept slots, ascending */
+  }
+  offs[U] = pos;
+  return U;
+}
+
+/* The verification pass of all n tokens under an expert budget: every token
+ * is routed, the kept experts are chosen from all n*k slots (the routed ids
+ * and their double gate weights), and each token's output sums its kept
+ * slots only (plus the shared expert).  keep: [N] out.  Returns the number
+ * of kept experts. */
+int orc_verify_budget(const orc_layer *L, const void *hs, int n, int n_threads,
+                      int budget, int32_t *ids, double *w, double *z,
+                      double *y, uint8_t *keep) {
+  run_workers(L, hs, NULL, n, n_threads, DO_ROUTE, NULL, ids, w, z, y);
+  double *score = (double *)malloc(sizeof(double) * (size_t)L->n_experts);
+  int kept = orc_expert_budget(ids, w, n * L->top_k, L->n_experts, budget, keep, score);
+  free(score);
+  run_workers(L, hs, NULL, n, n_threads, DO_FFN, keep, ids, w, z, y);
+  return kept;
 }

@@ -32,6 +32,19 @@ MUTANTS = {
     "plan_not_stable": ("for (int p = 0; p < n_slots; ++p)\n      if (ids[p] == uniq[u]) perm[pos++] = p;",
                         "for (int p = n_slots - 1; p >= 0; --p)\n      if (ids[p] == uniq[u]) perm[pos++] = p;"),
     "scale_bytes_dropped": ("*scales = (int64_t)4 *", "*scales = (int64_t)0 *"),
+    "budget_keeps_least_contribution": ("return x->score < y->score ? 1 : -1;",
+                                        "return x->score > y->score ? 1 : -1;"),
+    "budget_ties_to_higher_id": ("return x->id < y->id ? -1 : (x->id > y->id ? 1 : 0);",
+                                 "return x->id > y->id ? -1 : (x->id < y->id ? 1 : 0);"),
+    "budget_counts_slots_not_weights": ("score[ids[p]] += w[p];", "score[ids[p]] += 1.0;"),
+    "budget_one_too_few": ("int kept = U < budget ? U : budget;",
+                           "int kept = U < budget ? U : budget - 1;"),
+    "budget_dropped_slot_still_summed": ("if (keep && !keep[ids[j]]) continue;",
+                                         "if (0 && keep && !keep[ids[j]]) continue;"),
+    "budget_dropped_weight_kept": ("w_kept[p] = keep[ids[p]] ? w[p] : 0.0;", "w_kept[p] = w[p];"),
+    "budget_plan_counts_dropped": ("if (keep[ids[p]]) hist[ids[p]] += 1;", "hist[ids[p]] += 1;"),
+    "budget_plan_not_stable": ("for (int p = 0; p < n_slots; ++p)\n      if (uniq[u] == ids[p])",
+                               "for (int p = n_slots - 1; p >= 0; --p)\n      if (uniq[u] == ids[p])"),
 }
 
 

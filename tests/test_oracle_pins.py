@@ -357,3 +357,150 @@ def test_expert_bytes_printed_on_the_pages():
     assert wb == 9_437_184 and round(wb / 1e6, 1) == 9.4 and sb == 0
     # and 48 layers of it is about 0.45 GB
     assert round(48 * wb / 1e9, 2) == 0.45
+
+
+# ------------------------------------------------------------ expert budget
+# Verification-time expert budgeting (MoE-Spec, as its abstract is listed on
+# "Speculative Decoding for MoE Models: Expert Bytes, ..."; "The Limits of
+# Speculation", Sec. 2.4): keep the `budget` experts that contribute most,
+# drop the rest.  Contribution = summed gate weight (a reading).
+
+def test_budget_hand_worked_example():
+    # slots (token, slot): expert ids and weights
+    #   t0: e0 .625  e1 .375      contributions: e0 .625, e1 .375 + .75 = 1.125,
+    #   t1: e1 .75   e2 .25                      e2 .25 + .875 = 1.125, e3 .125
+    #   t2: e2 .875  e3 .125      e1 and e2 tie: the lower id ranks first
+    ids = np.array([[0, 1], [1, 2], [2, 3]], dtype=np.int32)
+    w = np.array([[.625, .375], [.75, .25], [.875, .125]])
+    keep, score, kept = O.expert_budget(ids, w, 5, 2)
+    assert score.tolist() == [.625, 1.125, 1.125, .125, 0.0]
+    assert keep.tolist() == [False, True, True, False, False] and kept == 2
+    assert O.expert_budget(ids, w, 5, 1)[0].tolist() == [False, True, False, False, False]
+    assert O.expert_budget(ids, w, 5, 3)[0].tolist() == [True, True, True, False, False]
+    assert O.expert_budget(ids, w, 5, 0)[2] == 0
+    # the kept plan: experts 1 and 2; slots 1, 2 (e1) and 3, 4 (e2)
+    U, hist, uniq, offs, perm, w_kept, _ = O.budget_plan(ids, w, 5, 2)
+    assert U == 2 and hist.tolist() == [0, 2, 2, 0, 0]
+    assert uniq.tolist() == [1, 2] and offs.tolist() == [0, 2, 4] and perm.tolist() == [1, 2, 3, 4]
+    assert w_kept.tolist() == [0.0, .375, .75, .25, .875, 0.0]
+
+
+def test_budget_brute_force_max_total_contribution():
+    # dyadic weights (multiples of 1/8) make every sum exact and create ties;
+    # the kept set must have the largest total contribution of any set of
+    # min(B, U) used experts, and must precede every dropped expert in the
+    # order (contribution descending, id ascending)
+    rng = np.random.default_rng(77)
+    for trial in range(60):
+        E = int(rng.integers(4, 11))
+        k = int(rng.integers(1, min(E, 4) + 1))
+        n = int(rng.integers(1, 6))
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(n)]).astype(np.int32)
+        w = rng.integers(1, 9, size=(n, k)) / 8.0
+        used = sorted(set(ids.ravel().tolist()))
+        contrib = {e: math.fsum(w.ravel()[ids.ravel() == e]) for e in used}
+        for B in range(0, len(used) + 2):
+            keep, score, kept = O.expert_budget(ids, w, E, B)
+            m = min(B, len(used))
+            assert kept == m and keep.sum() == m
+            for e in range(E):
+                assert score[e] == contrib.get(e, 0.0)
+            best = max((sum(contrib[e] for e in c) for c in itertools.combinations(used, m)),
+                       default=0.0)
+            assert sum(contrib[e] for e in used if keep[e]) == best
+            kept_ids = [e for e in used if keep[e]]
+            dropped = [e for e in used if not keep[e]]
+            for a in kept_ids:
+                for b in dropped:
+                    assert contrib[a] > contrib[b] or (contrib[a] == contrib[b] and a < b)
+            assert not keep[[e for e in range(E) if e not in contrib]].any()
+
+
+def test_budget_kept_sets_are_nested():
+    from moe_expert_ffn_gemv_gb300 import synth
+    ids = synth.uniform_ids(16, 8, 128, seed=5).numpy()
+    w = np.random.default_rng(6).random(ids.shape)
+    prev = np.zeros(128, dtype=bool)
+    for B in range(0, 129):
+        keep = O.expert_budget(ids, w, 128, B)[0]
+        assert np.all(keep[prev]) and keep.sum() == min(B, O.union_plan(ids, 128)[0])
+        prev = keep
+
+
+def test_budget_at_or_above_the_union_is_the_plain_plan():
+    rng = np.random.default_rng(8)
+    ids = np.stack([rng.permutation(64)[:8] for _ in range(12)]).astype(np.int32)
+    w = rng.random(ids.shape)
+    U, hist, uniq, offs, perm = O.union_plan(ids, 64)
+    for B in (U, U + 1, 64, 1000):
+        Ub, histb, uniqb, offsb, permb, w_kept, keep = O.budget_plan(ids, w, 64, B)
+        assert Ub == U and np.array_equal(histb, hist) and np.array_equal(uniqb, uniq)
+        assert np.array_equal(offsb, offs) and np.array_equal(permb, perm)
+        assert np.array_equal(w_kept, w.ravel())
+    # one below the union drops exactly the expert of least contribution
+    Ub, histb, uniqb, offsb, permb, w_kept, keep = O.budget_plan(ids, w, 64, U - 1)
+    score = O.expert_budget(ids, w, 64, U)[1]
+    least = min(uniq.tolist(), key=lambda e: (score[e], -e))
+    assert Ub == U - 1 and sorted(set(uniq.tolist()) - set(uniqb.tolist())) == [least]
+    assert np.all(w_kept[ids.ravel() == least] == 0.0) and permb.size == ids.size - hist[least]
+
+
+def test_budget_pass_equals_full_pass_with_dropped_experts_zeroed():
+    # a dropped expert's term is absent: the same as running the unbudgeted
+    # pass on a layer whose dropped experts have all-zero weights (the router
+    # does not read expert weights, so the routing is unchanged)
+    rng = np.random.default_rng(61)
+    d, I, E, k, n = 16, 8, 12, 3, 6
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    wg, w13, w2, h = f(E, d), f(E, 2 * I, d), f(E, d, I), f(n, d)
+    sh = (f(2 * I, d), f(d, I))
+    for gate in (O.GATE_SOFTMAX, O.GATE_SIGMOID_RENORM):
+        L = _f32_layer(d, I, E, k, gate, wg, w13, w2, sh)
+        ids, w, _, y_full = O.verify(L, h)
+        U = O.union_plan(ids, E)[0]
+        for B in (0, 1, 3, U - 1, U):
+            idsb, wb, _, yb, keep = O.verify_budget(L, h, B, threads=2)
+            assert np.array_equal(idsb, ids) and np.array_equal(wb, w)
+            assert np.array_equal(keep, O.expert_budget(ids, w, E, B)[0])
+            w13z, w2z = w13.copy(), w2.copy()
+            w13z[~keep] = 0.0
+            w2z[~keep] = 0.0
+            _, _, _, yz = O.verify(_f32_layer(d, I, E, k, gate, wg, w13z, w2z, sh), h)
+            assert np.array_equal(yb, yz), (gate, B)
+            if B >= U:
+                assert np.array_equal(yb, y_full)
+
+
+def test_budget_zero_leaves_only_the_shared_expert():
+    rng = np.random.default_rng(62)
+    d, I, E, k, n = 8, 4, 6, 2, 5
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    wg, w13, w2, h = f(E, d), f(E, 2 * I, d), f(E, d, I), f(n, d)
+    sh13, sh2 = f(2 * I, d), f(d, I)
+    y0 = O.verify_budget(_f32_layer(d, I, E, k, O.GATE_SOFTMAX, wg, w13, w2), h, 0)[3]
+    assert np.array_equal(y0, np.zeros((n, d)))
+    ys = O.verify(_f32_layer(d, I, 1, 1, O.GATE_SOFTMAX_RENORM, wg[:1], sh13[None], sh2[None]),
+                  h)[3]
+    y1 = O.verify_budget(_f32_layer(d, I, E, k, O.GATE_SOFTMAX, wg, w13, w2, (sh13, sh2)), h, 0)[3]
+    assert np.array_equal(y1, ys)
+
+
+def test_budget_e4m3_layer_zeroed_codes():
+    # the same identity on an FP8 layer with block scales: zero codes (+0)
+    # for the dropped experts, scales untouched
+    from moe_expert_ffn_gemv_gb300 import synth
+    from tests.helpers import np_bytes, oracle_layer
+    cfg = synth.LayerConfig("fp8-budget", 256, 8, 3, 128, synth.BF16, synth.E4M3,
+                            synth.GATE_SIGMOID_RENORM, n_shared=1)
+    layer = synth.make_layer(cfg, seed=12)
+    h = np_bytes(synth.make_hidden(cfg, 4, seed=13))
+    L = oracle_layer(layer)
+    U = O.union_plan(O.verify(L, h)[0], 8)[0]
+    assert U >= 4
+    for B in (1, 3):
+        _, _, _, yb, keep = O.verify_budget(L, h, B)
+        lz = synth.make_layer(cfg, seed=12)
+        lz.w13[torch.from_numpy(~keep)] = 0
+        lz.w2[torch.from_numpy(~keep)] = 0
+        _, _, _, yz = O.verify(oracle_layer(lz), h)
+        assert np.array_equal(yb, yz)
