@@ -63,6 +63,9 @@ def parse():
     p.add_argument("--fit-config", default=None, choices=sorted(synth.CONFIGS),
                    help="fit the bandwidth cost model on this layer shape and test it")
     p.add_argument("--windows", type=int, default=4, help="routing windows to fit (and to test)")
+    p.add_argument("--budget-config", default=None, choices=sorted(synth.CONFIGS),
+                   help="expert-budget sweep (MoE-Spec) on this layer shape, then exit")
+    p.add_argument("--budget-n", default="8,16,32,64", help="pass sizes of the budget sweep")
     p.add_argument("--rho", type=float, default=None, help="chain/tree correlation for the sweep")
     p.add_argument("--sigma", type=float, default=None, help="tree noise for the sweep")
     p.add_argument("--experts", type=int, default=None,
@@ -487,6 +490,74 @@ def run_sweep_only(args):
                       "hidden": cfg.hidden, **sw}))
 
 
+def run_budget(args):
+    """--budget-config NAME: the verification-time expert budget (MoE-Spec)
+    for n in --budget-n and B from the full union U down to a quarter of it
+    and k: µs of the fused route + budgeted plan (against the plain one), µs
+    and GB/s of the deduplicating expert call on the kept union bytes, and
+    how far the output moves from the unbudgeted output (the cap is lossy):
+    relative L2 distance and the largest element-relative deviation."""
+    from moe_expert_ffn_gemv_gb300 import binding as mv
+    torch.cuda.set_device(0)
+    cfg = synth.CONFIGS[args.budget_config]
+    layer = synth.make_layer(cfg, seed=1, device="cuda")
+    h_all = synth.make_hidden(cfg, 64, seed=3, device="cuda", rho=args.rho, sigma=args.sigma)
+    eb = sum(mv.moe_expert_bytes(mv.make_desc(cfg, 64)))
+    vl = mv.VerifyLayer(layer, 64)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    fa = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    fb = torch.ones_like(fa)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps=5):
+        ts = []
+        for _ in range(reps):
+            flush_l2(fa, fb)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    rows = []
+    for n in [int(x) for x in args.budget_n.split(",")]:
+        h = h_all[:n].contiguous()
+        vl.route_plan(h, n)
+        y_full = vl.dedup(h, n).float().clone()
+        U = int(vl.plan.n_uniq[0])
+        t_plan_plain = timed(lambda: vl.route_plan(h, n))
+        t_full = timed(lambda: vl.dedup(h, n))
+        budgets = sorted({U, (3 * U) // 4, U // 2, U // 4, cfg.top_k}, reverse=True)
+        for B in budgets:
+            vl.route_plan(h, n, budget=B)
+            y = vl.dedup(h, n, kept=True).float().clone()
+            Uk = int(vl.plan.n_uniq[0])
+            assert int(vl.routed_u[0]) == U and Uk == min(B, U)
+            t_plan = timed(lambda: vl.route_plan(h, n, budget=B))
+            t = timed(lambda: vl.dedup(h, n, kept=True))
+            kept_bytes = (Uk + cfg.n_shared) * eb
+            rms = float(y_full.pow(2).mean().sqrt())
+            dev = (y - y_full).abs() / torch.clamp(y_full.abs(), min=rms)
+            rows.append([n, U, B, round(1e6 * t_plan_plain, 1), round(1e6 * t_plan, 1),
+                         round(1e6 * t_full, 1), round(1e6 * t, 1),
+                         round(kept_bytes / t / 1e9, 1),
+                         round(1 - kept_bytes / ((U + cfg.n_shared) * eb), 3),
+                         float(f"{float((y - y_full).norm() / y_full.norm()):.4g}"),
+                         float(f"{float(dev.max()):.4g}")])
+    assert vl.last_error() == 0
+    print(json.dumps({
+        "budget_config": cfg.name, "rho": args.rho if args.rho is not None else cfg.rho,
+        "sigma": args.sigma if args.sigma is not None else cfg.sigma, "hidden": cfg.hidden,
+        "columns": ["n", "U", "B", "us_route_plan", "us_route_plan_budgeted", "us_dedup_full",
+                    "us_dedup_budgeted", "gbs_kept_union", "union_bytes_saved",
+                    "rel_l2_dev_from_full", "max_rel_dev_from_full"],
+        "rows": rows,
+        "l2": "flushed (2x L2 written then 2x L2 read) before each timed call; median of 5"}))
+
+
 # ------------------------------------------------------------- cpu / oracle
 
 def oracle_inputs(layer, h):
@@ -571,6 +642,8 @@ def main():
         WORKLOAD += f" ({args.experts} routed experts: profiling case)"
     if args.fit_config:
         run_fit(args)
+    elif args.budget_config:
+        run_budget(args)
     elif args.sweep_config:
         run_sweep_only(args)
     elif args.impl == "reference":

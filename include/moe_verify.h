@@ -22,6 +22,11 @@
  *          once per pass (union bytes U*b)                    (moe_verify_dedup)
  *        - per-slot: an expert's weights are read once per (token, slot)
  *          that names it (requested bytes n*k*b)            (moe_verify_perslot)
+ *   4. optionally, a verification-time expert budget (MoE-Spec, as "The
+ *      Limits of Speculation", Sec. 2.4 describes it): the plan keeps at
+ *      most B routed experts, those of largest summed gate weight, and the
+ *      dropped slots leave the output
+ *                         (moe_union_plan_budgeted, moe_route_plan_budgeted)
  *
  * Conventions shared by every call
  *   - Pointers named "device" are CUDA device pointers that the caller
@@ -200,6 +205,47 @@ moe_status moe_route_plan(const moe_layer_desc *desc, const void *router_w,
                           float *logits, const moe_plan *plan, void *workspace,
                           size_t ws_bytes, moe_stream_t stream);
 
+/* Verification-time expert budget (MoE-Spec, as its abstract is listed on
+ * "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes, Kernel
+ * Bandwidth and the Best Draft Length"; "The Limits of Speculation",
+ * Sec. 2.4: a cap on the experts loaded per layer, keeping those that
+ * contribute most and dropping the long tail).  moe_union_plan, except
+ * that at most `budget` routed experts enter the plan:
+ *   - an expert's contribution is the sum of the weights w of the slots
+ *     that name it, added in double in ascending slot order;
+ *   - when more than `budget` experts are used, the kept ones are the first
+ *     `budget` by (contribution descending, id ascending); otherwise all;
+ *   - `plan` is the plan of the kept slots only (a dropped expert has
+ *     hist 0, is not in uniq, and its slots are not in perm; offs[U] is the
+ *     number of kept slots; union_bytes counts the kept experts + shared);
+ *   - w_kept[p] = w[p] for a kept slot and 0 for a dropped slot (or an
+ *     invalid id).  Passing w_kept as the weights of moe_verify_dedup gives
+ *     the budgeted layer output: dropped terms are left out, the kept
+ *     weights are not renormalised, the shared expert is always applied.
+ *   w             device [n][k] float, the gate weights of ids
+ *   budget        >= 0 (0 keeps no routed expert); else MOE_ERR_INVALID_ARG
+ *   w_kept        device [n][k] float (out); may not alias w
+ *   routed_union  device int32 (out): U before the cap, or NULL
+ * The output is lossy whenever the cap drops an expert. */
+moe_status moe_union_plan_budgeted(const moe_layer_desc *desc,
+                                   const int32_t *ids, const float *w,
+                                   int32_t n, int32_t budget,
+                                   const moe_plan *plan, float *w_kept,
+                                   int32_t *routed_union, int32_t *error_word,
+                                   moe_stream_t stream);
+
+/* moe_route_plan with the budgeted plan of moe_union_plan_budgeted: one
+ * launch routes, gates, caps the union at `budget` experts and writes
+ * w_kept (and routed_union unless NULL).  Same outputs, bit for bit, as
+ * moe_route_topk followed by moe_union_plan_budgeted. */
+moe_status moe_route_plan_budgeted(const moe_layer_desc *desc,
+                                   const void *router_w, const void *h,
+                                   int32_t n, int32_t budget, int32_t *ids,
+                                   float *w, float *logits,
+                                   const moe_plan *plan, float *w_kept,
+                                   int32_t *routed_union, void *workspace,
+                                   size_t ws_bytes, moe_stream_t stream);
+
 /* The layer output with the deduplicating engine: every expert of the plan
  * (plus the shared expert) is applied once to all tokens routed to it, its
  * weights streamed from HBM once per pass, and
@@ -208,6 +254,8 @@ moe_status moe_route_plan(const moe_layer_desc *desc, const void *router_w,
  *   weights    the layer's experts (device pointers inside)
  *   h          device [n][d] act_dtype;   ids  device [n][k] int32
  *   w          device [n][k] float;       plan built by moe_union_plan from ids
+ *              (or w_kept and the plan of moe_union_plan_budgeted; a slot
+ *              of weight 0 is skipped in the sum)
  *   workspace  device, ws_bytes >= moe_workspace_bytes(desc)
  *   y          device [n][d] act_dtype (out)
  * The intermediate activations are kept in fp32 (F32 weights), bf16 (BF16

@@ -34,7 +34,8 @@ MOE_GATE_SOFTMAX, MOE_GATE_SOFTMAX_RENORM, MOE_GATE_SIGMOID_RENORM = 0, 1, 2
 EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_topk_from_logits",
             "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot", "moe_workspace_init",
             "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
-            "moe_pack_expert_weights", "moe_verify_dedup_noalloc", "moe_route_plan"]
+            "moe_pack_expert_weights", "moe_verify_dedup_noalloc", "moe_route_plan",
+            "moe_union_plan_budgeted", "moe_route_plan_budgeted"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -68,6 +69,13 @@ _lib.moe_union_plan.argtypes = [_D, _P, ctypes.c_int32, ctypes.POINTER(moe_plan)
 _lib.moe_route_plan.restype = ctypes.c_int
 _lib.moe_route_plan.argtypes = [_D, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.POINTER(moe_plan), _P,
                                 ctypes.c_size_t, _P]
+_lib.moe_union_plan_budgeted.restype = ctypes.c_int
+_lib.moe_union_plan_budgeted.argtypes = [_D, _P, _P, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.POINTER(moe_plan), _P, _P, _P, _P]
+_lib.moe_route_plan_budgeted.restype = ctypes.c_int
+_lib.moe_route_plan_budgeted.argtypes = [_D, _P, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
+                                         ctypes.POINTER(moe_plan), _P, _P, _P, ctypes.c_size_t,
+                                         _P]
 _lib.moe_verify_dedup.restype = ctypes.c_int
 _lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32, _P,
                                   _P, ctypes.POINTER(moe_plan), _P, ctypes.c_size_t, _P, _P]
@@ -149,6 +157,23 @@ def moe_route_plan(desc, router_w, h, n, ids, w, logits, plan: moe_plan, workspa
                                _ptr(logits), ctypes.byref(plan), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_route_plan")
+
+
+def moe_union_plan_budgeted(desc, ids, w, n, budget, plan: moe_plan, w_kept, routed_union=None,
+                            error_word=None, stream=None) -> None:
+    _check(_lib.moe_union_plan_budgeted(ctypes.byref(desc), _ptr(ids), _ptr(w), n, budget,
+                                        ctypes.byref(plan), _ptr(w_kept), _ptr(routed_union),
+                                        _ptr(error_word), _stream(stream)),
+           "moe_union_plan_budgeted")
+
+
+def moe_route_plan_budgeted(desc, router_w, h, n, budget, ids, w, logits, plan: moe_plan, w_kept,
+                            routed_union, workspace, stream=None) -> None:
+    _check(_lib.moe_route_plan_budgeted(ctypes.byref(desc), _ptr(router_w), _ptr(h), n, budget,
+                                        _ptr(ids), _ptr(w), _ptr(logits), ctypes.byref(plan),
+                                        _ptr(w_kept), _ptr(routed_union), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "moe_route_plan_budgeted")
 
 
 def moe_verify_dedup(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_plan, workspace,
@@ -291,24 +316,40 @@ class VerifyLayer:
                                 _aligned_empty(n_max * k, i32, device),
                                 _aligned_empty(1, torch.int64, device))
         self._cplan = self.plan.c()
+        self.w_kept = _aligned_empty(n_max * k, torch.float32, device)  # budgeted weights
+        self.routed_u = _aligned_empty(1, i32, device)                   # U before a budget
         self.error_word = self.workspace[:4].view(torch.int32)
         self.y = torch.empty(n_max, cfg.d, dtype=synth.torch_dtype(cfg.act), device=device)
 
     def route(self, h: torch.Tensor, n: int) -> None:
         moe_route_topk(self.desc, self.layer.wg, h, n, self.ids, self.w, self.logits)
 
-    def union_plan(self, n: int) -> None:
-        moe_union_plan(self.desc, self.ids, n, self._cplan, self.error_word)
+    def union_plan(self, n: int, budget: Optional[int] = None) -> None:
+        """The union plan of the routed ids; with `budget`, the plan of the
+        kept experts only, and self.w_kept / self.routed_u written."""
+        if budget is None:
+            moe_union_plan(self.desc, self.ids, n, self._cplan, self.error_word)
+        else:
+            moe_union_plan_budgeted(self.desc, self.ids, self.w, n, budget, self._cplan,
+                                    self.w_kept, self.routed_u, self.error_word)
 
-    def route_plan(self, h: torch.Tensor, n: int) -> None:
-        """route + union_plan in one launch."""
-        moe_route_plan(self.desc, self.layer.wg, h, n, self.ids, self.w, self.logits, self._cplan,
-                       self.workspace)
+    def route_plan(self, h: torch.Tensor, n: int, budget: Optional[int] = None) -> None:
+        """route + union_plan (budgeted when `budget` is given) in one launch."""
+        if budget is None:
+            moe_route_plan(self.desc, self.layer.wg, h, n, self.ids, self.w, self.logits,
+                           self._cplan, self.workspace)
+        else:
+            moe_route_plan_budgeted(self.desc, self.layer.wg, h, n, budget, self.ids, self.w,
+                                    self.logits, self._cplan, self.w_kept, self.routed_u,
+                                    self.workspace)
 
-    def dedup(self, h: torch.Tensor, n: int, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    def dedup(self, h: torch.Tensor, n: int, y: Optional[torch.Tensor] = None,
+              kept: bool = False) -> torch.Tensor:
+        """The deduplicating engine on the current plan; kept=True combines
+        with the budgeted weights self.w_kept."""
         y = self.y if y is None else y
-        moe_verify_dedup(self.desc, self.weights, h, n, self.ids, self.w, self._cplan,
-                         self.workspace, y)
+        moe_verify_dedup(self.desc, self.weights, h, n, self.ids, self.w_kept if kept else self.w,
+                         self._cplan, self.workspace, y)
         return y[:n]
 
     def perslot(self, h: torch.Tensor, n: int, y: Optional[torch.Tensor] = None) -> torch.Tensor:
@@ -317,33 +358,37 @@ class VerifyLayer:
         return y[:n]
 
     def verify_pass(self, h: torch.Tensor, n: int, engine: str = "dedup",
-                    y: Optional[torch.Tensor] = None) -> torch.Tensor:
-        """Route, plan and run the experts: one MoE verification pass."""
+                    y: Optional[torch.Tensor] = None,
+                    budget: Optional[int] = None) -> torch.Tensor:
+        """Route, plan and run the experts: one MoE verification pass (with
+        the deduplicating engine, optionally under an expert budget)."""
         if engine == "dedup":
-            self.route_plan(h, n)
-            return self.dedup(h, n, y)
+            self.route_plan(h, n, budget)
+            return self.dedup(h, n, y, kept=budget is not None)
+        assert budget is None, "the expert budget applies to the deduplicating engine"
         self.route(h, n)
         return self.perslot(h, n, y)
 
-    def capture(self, h: torch.Tensor, n: int, engine: str = "dedup"):
+    def capture(self, h: torch.Tensor, n: int, engine: str = "dedup",
+                budget: Optional[int] = None):
         """Record one verification pass (route, plan, experts, combine) on `h`
         (a fixed device buffer) into CUDA graphs; returns (route_and_plan,
         experts), two torch.cuda.CUDAGraph objects replayed in that order.
         Every call of the pass is asynchronous and host-sync free, so it can
         be captured; replays read whatever `h` holds and write self.y."""
         # one eager pass first: sets kernel attributes and warms the library
-        self.verify_pass(h, n, engine)
+        self.verify_pass(h, n, engine, budget=budget)
         torch.cuda.synchronize()
         g_route = torch.cuda.CUDAGraph()
         g_experts = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_route):
             if engine == "dedup":
-                self.route_plan(h, n)
+                self.route_plan(h, n, budget)
             else:
                 self.route(h, n)
         with torch.cuda.graph(g_experts):
             if engine == "dedup":
-                self.dedup(h, n)
+                self.dedup(h, n, kept=budget is not None)
             else:
                 self.perslot(h, n)
         return g_route, g_experts

@@ -271,58 +271,108 @@ MOE_API moe_status moe_topk_from_logits(const moe_layer_desc *desc, const float 
                                       static_cast<cudaStream_t>(stream)));
 }
 
-MOE_API moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids, int32_t n,
-                                  const moe_plan *plan, int32_t *error_word,
-                                  moe_stream_t stream) {
+namespace moe {
+namespace {
+
+moe_status check_plan(const moe_plan *plan) {
+  if (!plan || !plan->hist || !plan->uniq || !plan->n_uniq || !plan->offs || !plan->perm ||
+      !plan->union_bytes)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(plan->hist) || !aligned16(plan->uniq) || !aligned16(plan->offs) ||
+      !aligned16(plan->perm))
+    return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+// budget < 0: the plain plan (w, w_kept, routed_u unused).
+moe_status union_plan(const moe_layer_desc *desc, const int32_t *ids, const float *w, int32_t n,
+                      int32_t budget, const moe_plan *plan, float *w_kept, int32_t *routed_u,
+                      int32_t *error_word, cudaStream_t st) {
   moe_status s = check_desc(desc);
   if (s != MOE_OK) return s;
   if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
-  if (!plan || !plan->hist || !plan->uniq || !plan->n_uniq || !plan->offs || !plan->perm ||
-      !plan->union_bytes || (n > 0 && !ids))
-    return MOE_ERR_INVALID_ARG;
-  if ((ids && !aligned16(ids)) || !aligned16(plan->hist) || !aligned16(plan->uniq) ||
-      !aligned16(plan->offs) || !aligned16(plan->perm))
+  if ((s = check_plan(plan)) != MOE_OK) return s;
+  if (n > 0 && (!ids || (budget >= 0 && (!w || !w_kept)))) return MOE_ERR_INVALID_ARG;
+  if ((ids && !aligned16(ids)) || (w && !aligned16(w)) || (w_kept && !aligned16(w_kept)))
     return MOE_ERR_ALIGNMENT;
   int64_t wb, sb;
   expert_bytes(*desc, &wb, &sb);
-  return cuda_status(launch_union_plan(ids, n * desc->top_k, desc->n_experts, desc->n_shared,
-                                       wb + sb, plan->hist, plan->uniq, plan->n_uniq, plan->offs,
-                                       plan->perm, plan->union_bytes, error_word,
-                                       static_cast<cudaStream_t>(stream)));
+  const int n_slots = n * desc->top_k;
+  if (budget < 0)
+    return cuda_status(launch_union_plan(ids, n_slots, desc->n_experts, desc->n_shared, wb + sb,
+                                         plan->hist, plan->uniq, plan->n_uniq, plan->offs,
+                                         plan->perm, plan->union_bytes, error_word, st));
+  return cuda_status(launch_union_plan_budgeted(
+      ids, w, n_slots, desc->n_experts, desc->n_shared, wb + sb, budget, plan->hist, plan->uniq,
+      plan->n_uniq, plan->offs, plan->perm, plan->union_bytes, w_kept, routed_u, error_word, st));
+}
+
+moe_status route_plan(const moe_layer_desc *desc, const void *router_w, const void *h, int32_t n,
+                      int32_t budget, int32_t *ids, float *w, float *logits, const moe_plan *plan,
+                      float *w_kept, int32_t *routed_u, void *workspace, size_t ws_bytes,
+                      cudaStream_t st) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
+  if ((s = check_plan(plan)) != MOE_OK) return s;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  int64_t wb, sb;
+  expert_bytes(*desc, &wb, &sb);
+  uint8_t *wsb = static_cast<uint8_t *>(workspace);
+  int32_t *err = reinterpret_cast<int32_t *>(wsb);
+  if (n == 0)  // the empty plan: U = 0, offs[0] = 0
+    return union_plan(desc, nullptr, nullptr, 0, budget, plan, nullptr, routed_u, err, st);
+  if (!router_w || !h || !ids || !w || !logits || (budget >= 0 && !w_kept))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(router_w) || !aligned16(h) || !aligned16(ids) || !aligned16(w) ||
+      !aligned16(logits) || (w_kept && !aligned16(w_kept)))
+    return MOE_ERR_ALIGNMENT;
+  return cuda_status(launch_route_plan(
+      desc->act_dtype == MOE_BF16, router_w, h, n, desc->d, desc->n_experts, desc->top_k,
+      desc->gate, desc->n_shared, wb + sb, logits, ids, w, plan->hist, plan->uniq, plan->n_uniq,
+      plan->offs, plan->perm, plan->union_bytes, budget, w_kept, routed_u, err,
+      reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET), st));
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_API moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids, int32_t n,
+                                  const moe_plan *plan, int32_t *error_word,
+                                  moe_stream_t stream) {
+  return union_plan(desc, ids, nullptr, n, -1, plan, nullptr, nullptr, error_word,
+                    static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_union_plan_budgeted(const moe_layer_desc *desc, const int32_t *ids,
+                                           const float *w, int32_t n, int32_t budget,
+                                           const moe_plan *plan, float *w_kept,
+                                           int32_t *routed_union, int32_t *error_word,
+                                           moe_stream_t stream) {
+  if (budget < 0) return MOE_ERR_INVALID_ARG;
+  return union_plan(desc, ids, w, n, budget, plan, w_kept, routed_union, error_word,
+                    static_cast<cudaStream_t>(stream));
 }
 
 MOE_API moe_status moe_route_plan(const moe_layer_desc *desc, const void *router_w, const void *h,
                                   int32_t n, int32_t *ids, float *w, float *logits,
                                   const moe_plan *plan, void *workspace, size_t ws_bytes,
                                   moe_stream_t stream) {
-  moe_status s = check_desc(desc);
-  if (s != MOE_OK) return s;
-  if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
-  if (!plan || !plan->hist || !plan->uniq || !plan->n_uniq || !plan->offs || !plan->perm ||
-      !plan->union_bytes || !workspace)
-    return MOE_ERR_INVALID_ARG;
-  if (!aligned16(plan->hist) || !aligned16(plan->uniq) || !aligned16(plan->offs) ||
-      !aligned16(plan->perm) || !aligned16(workspace))
-    return MOE_ERR_ALIGNMENT;
-  if (ws_bytes < 256) return MOE_ERR_WORKSPACE;
-  int64_t wb, sb;
-  expert_bytes(*desc, &wb, &sb);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t *wsb = static_cast<uint8_t *>(workspace);
-  int32_t *err = reinterpret_cast<int32_t *>(wsb);
-  if (n == 0)  // the empty plan: U = 0, offs[0] = 0
-    return cuda_status(launch_union_plan(nullptr, 0, desc->n_experts, desc->n_shared, wb + sb,
-                                         plan->hist, plan->uniq, plan->n_uniq, plan->offs,
-                                         plan->perm, plan->union_bytes, err, st));
-  if (!router_w || !h || !ids || !w || !logits) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(router_w) || !aligned16(h) || !aligned16(ids) || !aligned16(w) ||
-      !aligned16(logits))
-    return MOE_ERR_ALIGNMENT;
-  return cuda_status(launch_route_plan(
-      desc->act_dtype == MOE_BF16, router_w, h, n, desc->d, desc->n_experts, desc->top_k,
-      desc->gate, desc->n_shared, wb + sb, logits, ids, w, plan->hist, plan->uniq, plan->n_uniq,
-      plan->offs, plan->perm, plan->union_bytes, err,
-      reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET), st));
+  return route_plan(desc, router_w, h, n, -1, ids, w, logits, plan, nullptr, nullptr, workspace,
+                    ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_route_plan_budgeted(const moe_layer_desc *desc, const void *router_w,
+                                           const void *h, int32_t n, int32_t budget,
+                                           int32_t *ids, float *w, float *logits,
+                                           const moe_plan *plan, float *w_kept,
+                                           int32_t *routed_union, void *workspace,
+                                           size_t ws_bytes, moe_stream_t stream) {
+  if (budget < 0) return MOE_ERR_INVALID_ARG;
+  return route_plan(desc, router_w, h, n, budget, ids, w, logits, plan, w_kept, routed_union,
+                    workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 MOE_API moe_status moe_verify_dedup(const moe_layer_desc *desc, const moe_expert_weights *weights,

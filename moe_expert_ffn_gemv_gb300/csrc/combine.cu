@@ -5,10 +5,13 @@
 // combine_kernel: y[t][c] = sum_{j<k} w[t][j] * yslot[t*k+j][c]
 //                           (+ yslot[n*k+t][c] for the shared expert),
 // fp32 fused multiply-adds in that fixed order, then one rounding to the
-// output dtype (round to nearest even for bf16).  Each thread owns 4
-// consecutive columns of one token (16-byte loads, all slots' loads issued
-// before the multiply-adds); small CTAs so that a pass of a few tokens still
-// spreads over the SMs.
+// output dtype (round to nearest even for bf16).  A slot whose weight is 0
+// is skipped, not multiplied: an expert budget leaves a dropped slot's
+// yslot row unwritten and gives it weight 0.  (Skipping changes no sum:
+// the accumulator starts at +0 and adding 0 * finite leaves it as it is.)
+// Each thread owns 4 consecutive columns of one token (16-byte loads, all
+// slots' loads issued before the multiply-adds); small CTAs so that a pass
+// of a few tokens still spreads over the SMs.
 #include "kernels.h"
 #include "moe_common.cuh"
 
@@ -41,7 +44,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const float *_
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      if (j0 + q < k) {
+      if (j0 + q < k && wt[q] != 0.f) {
         acc.x = fmaf(wt[q], v[q].x, acc.x);
         acc.y = fmaf(wt[q], v[q].y, acc.y);
         acc.z = fmaf(wt[q], v[q].z, acc.z);

@@ -59,18 +59,28 @@ cudaError_t launch_topk_gate(const float *logits, int n, int n_experts, int k, i
                              int32_t *ids, float *w, cudaStream_t stream);
 
 // Router scores + top-k + gate + union plan in one launch; `counter` is a
-// zeroed device word that the kernel leaves zeroed.
+// zeroed device word that the kernel leaves zeroed.  budget >= 0: the
+// budgeted plan (w_kept written, routed_u if not NULL); budget < 0: none.
 cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, int n, int d,
                               int n_experts, int k, int gate, int n_shared, int64_t expert_bytes,
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
-                              int32_t *err, unsigned int *counter, cudaStream_t stream);
+                              int budget, float *w_kept, int32_t *routed_u, int32_t *err,
+                              unsigned int *counter, cudaStream_t stream);
 
 // Expert union and slot permutation (one CTA).
 cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, int n_shared,
                               int64_t expert_bytes, int32_t *hist, int32_t *uniq, int32_t *n_uniq,
                               int32_t *offs, int32_t *perm, int64_t *union_bytes, int32_t *err,
                               cudaStream_t stream);
+
+// The same under an expert budget (budget >= 0): see union_plan_block.
+cudaError_t launch_union_plan_budgeted(const int32_t *ids, const float *w, int n_slots,
+                                       int n_experts, int n_shared, int64_t expert_bytes,
+                                       int budget, int32_t *hist, int32_t *uniq, int32_t *n_uniq,
+                                       int32_t *offs, int32_t *perm, int64_t *union_bytes,
+                                       float *w_kept, int32_t *routed_u, int32_t *err,
+                                       cudaStream_t stream);
 
 // y[t] = sum_j w[t][j] yslot[t*k+j] (+ yslot[n*k+t]) -> y (fp32 or bf16).
 cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,

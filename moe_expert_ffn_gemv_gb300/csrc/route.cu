@@ -124,13 +124,15 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict_
 // computes its (expert, 8-token) scores as router_scores_kernel does, then
 // takes a ticket; the CTA that takes the last ticket (so all scores are
 // written) runs the top-k of every token (one warp per token) and then
-// union_plan_block, and resets the ticket counter for the next call.
-template <typename T>
+// union_plan_block (BUDGET: the budgeted plan), and resets the ticket
+// counter for the next call.
+template <typename T, bool BUDGET>
 __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
     const T *__restrict__ wg, const T *__restrict__ h, int n, int d, int n_experts, int k,
     int gate, int n_shared, int64_t expert_bytes, float *logits, int32_t *ids, float *w,
     int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
-    int64_t *union_bytes, int32_t *err, unsigned int *counter) {
+    int64_t *union_bytes, int budget, float *w_kept, int32_t *routed_u, int32_t *err,
+    unsigned int *counter) {
   router_scores_cta(wg, h, n, d, n_experts, logits);
   __shared__ int s_last;
   __syncthreads();
@@ -146,10 +148,17 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
   for (int t = warp; t < n; t += n_warps)
     topk_gate_warp(logits + int64_t(t) * n_experts, n_experts, k, gate, ids + int64_t(t) * k,
                    w + int64_t(t) * k);
-  __syncthreads();  // ids of all tokens visible to the whole CTA
+  __syncthreads();  // ids and weights of all tokens visible to the whole CTA
   __shared__ PlanSmem S;
-  union_plan_block(S, ids, n * k, n_experts, n_shared, expert_bytes, hist, uniq, n_uniq, offs,
-                   perm, union_bytes, err);
+  if constexpr (BUDGET) {
+    __shared__ BudgetSmem B;
+    union_plan_block<true>(S, &B, ids, w, n * k, n_experts, n_shared, expert_bytes, budget, hist,
+                           uniq, n_uniq, offs, perm, union_bytes, w_kept, routed_u, err);
+  } else {
+    union_plan_block<false>(S, nullptr, ids, nullptr, n * k, n_experts, n_shared, expert_bytes,
+                            0, hist, uniq, n_uniq, offs, perm, union_bytes, nullptr, nullptr,
+                            err);
+  }
   if (threadIdx.x == 0) *counter = 0u;
 }
 
@@ -183,19 +192,31 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
                               int n_experts, int k, int gate, int n_shared, int64_t expert_bytes,
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
-                              int32_t *err, unsigned int *counter, cudaStream_t stream) {
+                              int budget, float *w_kept, int32_t *routed_u, int32_t *err,
+                              unsigned int *counter, cudaStream_t stream) {
   dim3 grid(n_experts, (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
-  const int warps = router_warps(d);
-  if (bf16)
-    route_plan_kernel<__nv_bfloat16><<<grid, warps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(router_w), static_cast<const __nv_bfloat16 *>(h), n, d,
-        n_experts, k, gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, perm,
-        union_bytes, err, counter);
-  else
-    route_plan_kernel<float><<<grid, warps * 32, 0, stream>>>(
-        static_cast<const float *>(router_w), static_cast<const float *>(h), n, d, n_experts, k,
-        gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, perm, union_bytes,
-        err, counter);
+  const int threads = router_warps(d) * 32;
+  const __nv_bfloat16 *wb = static_cast<const __nv_bfloat16 *>(router_w);
+  const __nv_bfloat16 *hb = static_cast<const __nv_bfloat16 *>(h);
+  const float *wf = static_cast<const float *>(router_w);
+  const float *hf = static_cast<const float *>(h);
+#define MOE_ROUTE_PLAN_ARGS                                                                  \
+  n, d, n_experts, k, gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, \
+      perm, union_bytes, budget, w_kept, routed_u, err, counter
+  if (budget < 0) {
+    if (bf16)
+      route_plan_kernel<__nv_bfloat16, false><<<grid, threads, 0, stream>>>(wb, hb,
+                                                                           MOE_ROUTE_PLAN_ARGS);
+    else
+      route_plan_kernel<float, false><<<grid, threads, 0, stream>>>(wf, hf, MOE_ROUTE_PLAN_ARGS);
+  } else {
+    if (bf16)
+      route_plan_kernel<__nv_bfloat16, true><<<grid, threads, 0, stream>>>(wb, hb,
+                                                                          MOE_ROUTE_PLAN_ARGS);
+    else
+      route_plan_kernel<float, true><<<grid, threads, 0, stream>>>(wf, hf, MOE_ROUTE_PLAN_ARGS);
+  }
+#undef MOE_ROUTE_PLAN_ARGS
   return cudaGetLastError();
 }
 

@@ -95,49 +95,44 @@ struct PlanSmem {
   int32_t ids[PLAN_MAX_SLOTS];
   int32_t warp_cnt[8];
   int32_t warp_sum[8];
+  int32_t n_uniq;
+  int32_t total;
 };
 
-// The whole block (blockDim.x >= 256, a multiple of 32): the expert union of
-// the n_slots routed ids and the grouping of the slots by expert
-// ("Less Experts, Faster Decoding", eq. (1); "Making Every Verified Token
-// Count", eq. (5); "The Limits of Speculation", App. A.4.1, eq. (A2)):
-//   1. histogram with shared-memory atomics;
-//   2. the used experts compacted in ascending order: warp w ballots experts
-//      32w..32w+31, __popc of the ballot below a lane gives the rank inside
-//      the warp, a scan over the 8 warp counts gives the warp base;
-//   3. exclusive prefix sum of the histogram (warp shuffle scan + warp
-//      totals) gives each expert's group offset;
-//   4. stable scatter: slot p goes to offs[ids[p]] + (earlier slots with the
-//      same id), so slots stay ascending inside a group;
-//   5. U and the union bytes (U + n_shared) * expert bytes.
-// `ids` may be written by this block just before (after a __syncthreads).
-__device__ __forceinline__ void union_plan_block(PlanSmem &S, const int32_t *ids, int n_slots,
-                                                 int n_experts, int n_shared, int64_t expert_bytes,
-                                                 int32_t *hist, int32_t *uniq, int32_t *n_uniq,
-                                                 int32_t *offs, int32_t *perm,
-                                                 int64_t *union_bytes, int32_t *err) {
+// Extra shared memory of the budgeted plan.
+struct BudgetSmem {
+  int32_t perm[PLAN_MAX_SLOTS];   // the grouping of all valid slots
+  float w[PLAN_MAX_SLOTS];        // the slots' gate weights
+  unsigned long long key[256];    // order key of the contribution of the used expert of rank r
+  int32_t expert[256];            // the used expert of rank r
+  int32_t keep[256];              // by expert id
+};
+
+// What thread e (< 256) knows of expert e after plan_scan.
+struct ExpertScan {
+  int cnt;   // slots naming e
+  int off;   // first position of e's group
+  int rank;  // position of e among the used experts (valid when cnt > 0)
+};
+
+// Exclusive scan of S.hist and the compaction of the used experts: warp w
+// ballots experts 32w..32w+31, __popc of the ballot below a lane gives the
+// rank inside the warp, a shuffle scan gives the offsets inside the warp and
+// the 8 warp totals give the bases.  Writes S.n_uniq (U) and S.total (the
+// slots counted).  Every thread of the block calls it.
+__device__ __forceinline__ ExpertScan plan_scan(PlanSmem &S, int n_experts) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 256) S.hist[tid] = 0;
-  __syncthreads();
-  for (int p = tid; p < n_slots; p += blockDim.x) {
-    const int e = ids[p];
-    const bool ok = e >= 0 && e < n_experts;
-    S.ids[p] = ok ? e : -1;
-    if (ok) atomicAdd(&S.hist[e], 1);
-    else record_error(err, MOE_ERR_DEVICE_INPUT);
-  }
-  __syncthreads();
-  int incl = 0, cnt = 0;
+  ExpertScan x{0, 0, 0};
+  int incl = 0;
   unsigned used = 0;
-  if (tid < 256) {  // warps 0..7: thread e handles expert e
-    const int e = tid;
-    cnt = e < n_experts ? S.hist[e] : 0;
-    used = __ballot_sync(0xffffffffu, cnt > 0);
-    incl = cnt;
+  if (tid < 256) {
+    x.cnt = tid < n_experts ? S.hist[tid] : 0;
+    used = __ballot_sync(0xffffffffu, x.cnt > 0);
+    incl = x.cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
     if (lane == 31) {
       S.warp_cnt[warp] = __popc(used);
@@ -146,38 +141,154 @@ __device__ __forceinline__ void union_plan_block(PlanSmem &S, const int32_t *ids
   }
   __syncthreads();
   if (tid < 256) {
-    const int e = tid;
-    int rank_base = 0, off_base = 0, U = 0;
+    int rank_base = 0, off_base = 0, U = 0, total = 0;
     for (int w = 0; w < 8; ++w) {
       if (w < warp) {
         rank_base += S.warp_cnt[w];
         off_base += S.warp_sum[w];
       }
       U += S.warp_cnt[w];
+      total += S.warp_sum[w];
     }
-    const int off = off_base + incl - cnt;
-    S.offs[e] = off;
-    if (e < n_experts) hist[e] = cnt;
-    if (cnt > 0) {
-      const int r = rank_base + __popc(used & ((1u << lane) - 1u));
-      uniq[r] = e;
-      offs[r] = off;
-    }
+    x.off = off_base + incl - x.cnt;
+    x.rank = rank_base + __popc(used & ((1u << lane) - 1u));
     if (tid == 0) {
-      int total = 0;
-      for (int w = 0; w < 8; ++w) total += S.warp_sum[w];
-      offs[U] = total;
-      *n_uniq = U;
-      *union_bytes = int64_t(U + n_shared) * expert_bytes;
+      S.n_uniq = U;
+      S.total = total;
     }
   }
+  __syncthreads();
+  return x;
+}
+
+// An unsigned integer with the order of the double s (for s not NaN): the
+// sign bit flipped for s >= 0, all bits flipped for s < 0, and -0 taken as
+// +0 so that equal contributions give equal keys.  Ranking on the key costs
+// integer compares instead of fp64 ones.
+__device__ __forceinline__ unsigned long long order_key(double s) {
+  if (s == 0.0) s = 0.0;
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(s));
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+
+// (key a, expert e) ranks before (key b, expert f): larger contribution, or
+// equal and lower id.
+__device__ __forceinline__ bool budget_beats(unsigned long long a, int e, unsigned long long b,
+                                             int f) {
+  return a > b || (a == b && e < f);
+}
+
+// The whole block (blockDim.x >= 256, a multiple of 32): the expert union of
+// the n_slots routed ids and the grouping of the slots by expert
+// ("Less Experts, Faster Decoding", eq. (1); "Making Every Verified Token
+// Count", eq. (5); "The Limits of Speculation", App. A.4.1, eq. (A2)):
+//   1. histogram with shared-memory atomics;
+//   2. plan_scan: the used experts in ascending order and their offsets;
+//   3. stable scatter: slot p goes to offs[ids[p]] + (earlier slots with the
+//      same id), so slots stay ascending inside a group;
+//   4. U and the union bytes (U + n_shared) * expert bytes.
+// BUDGET: at most `budget` routed experts are kept (MoE-Spec's per-layer
+// expert cap).  The weights are staged in shared memory with the ids.  When
+// U > budget, each used expert's contribution is the sum of its slots'
+// weights w[p], added in double in ascending slot order (its group in the
+// full grouping); the kept experts are the first `budget` by
+// (contribution descending, id ascending); the plan is rebuilt over the kept
+// slots only, and w_kept[p] = w[p] for a kept slot, 0 for a dropped one (or
+// an invalid id).  routed_u (may be NULL) receives U before the cut.
+// `ids` and `w` may be written by this block just before (after a
+// __syncthreads), so they are read with plain loads.
+template <bool BUDGET>
+__device__ __forceinline__ void union_plan_block(
+    PlanSmem &S, BudgetSmem *B, const int32_t *ids, const float *w, int n_slots, int n_experts,
+    int n_shared, int64_t expert_bytes, int budget, int32_t *hist, int32_t *uniq,
+    int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes, float *w_kept,
+    int32_t *routed_u, int32_t *err) {
+  const int tid = threadIdx.x;
+  if (tid < 256) S.hist[tid] = 0;
+  __syncthreads();
+  for (int p = tid; p < n_slots; p += blockDim.x) {
+    const int e = ids[p];
+    const bool ok = e >= 0 && e < n_experts;
+    S.ids[p] = ok ? e : -1;
+    if constexpr (BUDGET) B->w[p] = w[p];
+    if (ok) atomicAdd(&S.hist[e], 1);
+    else record_error(err, MOE_ERR_DEVICE_INPUT);
+  }
+  __syncthreads();
+  ExpertScan x = plan_scan(S, n_experts);
+  if (tid < 256) S.offs[tid] = x.off;
+  const bool cut = BUDGET && S.n_uniq > budget;
+  if (BUDGET && tid == 0 && routed_u) *routed_u = S.n_uniq;
+  int32_t *group = cut ? B->perm : perm;  // where the full grouping goes
   __syncthreads();
   for (int p = tid; p < n_slots; p += blockDim.x) {
     const int id = S.ids[p];
     if (id < 0) continue;
     int before = 0;
     for (int q = 0; q < p; ++q) before += S.ids[q] == id;
-    perm[S.offs[id] + before] = p;
+    group[S.offs[id] + before] = p;
+  }
+  if constexpr (BUDGET) {
+    if (cut) {
+      __syncthreads();  // the grouping in B->perm is complete
+      const int e = tid;
+      const int U = S.n_uniq;
+      unsigned long long mine = 0;
+      if (e < 256 && x.cnt > 0) {
+        double sum = 0.0;
+        for (int i = 0; i < x.cnt; ++i) sum += double(B->w[B->perm[x.off + i]]);
+        mine = order_key(sum);
+        B->key[x.rank] = mine;
+        B->expert[x.rank] = e;
+      }
+      __syncthreads();
+      int keep = 0;
+      if (e < 256 && x.cnt > 0) {
+        int r = 0;  // used experts that rank before e
+        for (int q = 0; q < U; ++q) r += budget_beats(B->key[q], B->expert[q], mine, e);
+        keep = r < budget;
+      }
+      if (e < 256) {
+        B->keep[e] = keep;
+        if (!keep) S.hist[e] = 0;
+      }
+      __syncthreads();
+      for (int p = tid; p < n_slots; p += blockDim.x) {
+        const int id = S.ids[p];
+        w_kept[p] = (id >= 0 && B->keep[id]) ? B->w[p] : 0.f;
+      }
+      const ExpertScan full = x;
+      x = plan_scan(S, n_experts);  // the kept experts only
+      if (tid < 256) {
+        if (e < n_experts) hist[e] = x.cnt;
+        if (x.cnt > 0) {
+          uniq[x.rank] = e;
+          offs[x.rank] = x.off;
+          for (int i = 0; i < x.cnt; ++i) perm[x.off + i] = B->perm[full.off + i];
+        }
+        if (tid == 0) {
+          offs[S.n_uniq] = S.total;
+          *n_uniq = S.n_uniq;
+          *union_bytes = int64_t(S.n_uniq + n_shared) * expert_bytes;
+        }
+      }
+      return;
+    }
+    for (int p = tid; p < n_slots; p += blockDim.x)
+      w_kept[p] = S.ids[p] >= 0 ? B->w[p] : 0.f;
+  }
+  if (tid < 256) {
+    const int e = tid;
+    if (e < n_experts) hist[e] = x.cnt;
+    if (x.cnt > 0) {
+      uniq[x.rank] = e;
+      offs[x.rank] = x.off;
+    }
+    if (tid == 0) {
+      offs[S.n_uniq] = S.total;
+      *n_uniq = S.n_uniq;
+      *union_bytes = int64_t(S.n_uniq + n_shared) * expert_bytes;
+    }
   }
 }
 

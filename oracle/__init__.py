@@ -84,8 +84,8 @@ def lib():
         L.orc_budget_plan.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       p, p, p, p, p, p, p]
         L.orc_verify_budget.restype = ctypes.c_int
-        L.orc_verify_budget.argtypes = [ctypes.POINTER(_Layer), p, ctypes.c_int, ctypes.c_int,
-                                        ctypes.c_int, p, p, p, p, p]
+        L.orc_verify_budget.argtypes = [ctypes.POINTER(_Layer), p, ctypes.c_int, p, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, p, p, p, p, p]
         _lib = L
     return _lib
 
@@ -267,20 +267,28 @@ def budget_plan(ids: np.ndarray, w: np.ndarray, n_experts: int, budget: int):
             w_kept[:flat.size].copy(), keep.astype(bool))
 
 
-def verify_budget(layer: Layer, h: np.ndarray, budget: int, threads: int = 1):
-    """The pass of all n tokens under an expert budget: (ids [n][k], w [n][k]
-    f64, z [n][N] f64, y [n][d] f64, keep [N] bool).  Routing is the same as
-    verify(); each token's output sums only its slots whose expert is kept
-    (plus the shared expert), with the weights not renormalised."""
+def verify_budget(layer: Layer, h: np.ndarray, budget: int, tokens=None, threads: int = 1):
+    """The pass of n tokens under an expert budget: (ids [n][k], w [n][k]
+    f64, z [n][N] f64, y [m][d] f64, keep [N] bool).  Routing is the same as
+    verify() and covers all n tokens (the kept experts depend on all of
+    them); y row i is token tokens[i] (all tokens if None) and sums only its
+    slots whose expert is kept (plus the shared expert), with the weights not
+    renormalised."""
     h = np.ascontiguousarray(h)
     n = h.shape[0]
     assert budget >= 0
+    if tokens is None:
+        tok, m = None, n
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        assert tok.size == 0 or (tok.min() >= 0 and tok.max() < n)
+        m = tok.shape[0]
     ids = np.zeros((n, layer.top_k), dtype=np.int32)
     w = np.zeros((n, layer.top_k), dtype=np.float64)
     z = np.zeros((n, layer.n_experts), dtype=np.float64)
-    y = np.zeros((n, layer.d), dtype=np.float64)
+    y = np.zeros((m, layer.d), dtype=np.float64)
     keep = np.zeros(layer.n_experts, dtype=np.uint8)
     c = layer._c()
-    lib().orc_verify_budget(ctypes.byref(c), _ptr(h), n, threads, budget, _ptr(ids), _ptr(w),
-                            _ptr(z), _ptr(y), _ptr(keep))
+    lib().orc_verify_budget(ctypes.byref(c), _ptr(h), n, _ptr(tok), m, threads, budget, _ptr(ids),
+                            _ptr(w), _ptr(z), _ptr(y), _ptr(keep))
     return ids, w, z, y, keep.astype(bool)

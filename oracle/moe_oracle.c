@@ -494,18 +494,36 @@ int orc_budget_plan(const int32_t *ids, const double *w, int n_slots,
   return U;
 }
 
-/* The verification pass of all n tokens under an expert budget: every token
- * is routed, the kept experts are chosen from all n*k slots (the routed ids
- * and their double gate weights), and each token's output sums its kept
- * slots only (plus the shared expert).  keep: [N] out.  Returns the number
- * of kept experts. */
-int orc_verify_budget(const orc_layer *L, const void *hs, int n, int n_threads,
+/* The verification pass of n tokens under an expert budget: every token is
+ * routed, the kept experts are chosen from all n*k slots (the routed ids and
+ * their double gate weights), and each output sums its token's kept slots
+ * only (plus the shared expert).  Outputs are written for the tokens listed
+ * in `tokens` (all n in order when NULL; then n_tokens = n): y row i belongs
+ * to token tokens[i]; ids, w, z hold all n tokens.  keep: [N] out.  Returns
+ * the number of kept experts. */
+int orc_verify_budget(const orc_layer *L, const void *hs, int n,
+                      const int32_t *tokens, int n_tokens, int n_threads,
                       int budget, int32_t *ids, double *w, double *z,
                       double *y, uint8_t *keep) {
-  run_workers(L, hs, NULL, n, n_threads, DO_ROUTE, NULL, ids, w, z, y);
+  run_workers(L, hs, NULL, n, n_threads, DO_ROUTE, NULL, ids, w, z, NULL);
   double *score = (double *)malloc(sizeof(double) * (size_t)L->n_experts);
   int kept = orc_expert_budget(ids, w, n * L->top_k, L->n_experts, budget, keep, score);
   free(score);
-  run_workers(L, hs, NULL, n, n_threads, DO_FFN, keep, ids, w, z, y);
+  if (!tokens) {
+    run_workers(L, hs, NULL, n, n_threads, DO_FFN, keep, ids, w, z, y);
+    return kept;
+  }
+  /* the listed tokens' routing, gathered in list order */
+  int k = L->top_k;
+  int32_t *ids_l = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_tokens * k + 1));
+  double *w_l = (double *)malloc(sizeof(double) * (size_t)(n_tokens * k + 1));
+  for (int i = 0; i < n_tokens; ++i)
+    for (int j = 0; j < k; ++j) {
+      ids_l[(size_t)i * k + j] = ids[(size_t)tokens[i] * k + j];
+      w_l[(size_t)i * k + j] = w[(size_t)tokens[i] * k + j];
+    }
+  run_workers(L, hs, tokens, n_tokens, n_threads, DO_FFN, keep, ids_l, w_l, NULL, y);
+  free(w_l);
+  free(ids_l);
   return kept;
 }

@@ -115,3 +115,33 @@ def test_status_strings(lib):
     for s in range(8):
         assert lib.moe_status_string(s) not in ("", "unknown status")
     assert lib.moe_status_string(99) == "unknown status"
+
+
+def test_budgeted_plan_calls_reject_bad_arguments_before_any_launch(lib):
+    D = _desc(lib)
+    P = ctypes.c_void_p
+    r = lib._lib
+    s0 = P(0)
+    y = P(0x1000)
+    plan = lib.moe_plan(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    nb = lib.moe_workspace_bytes(D)
+    # a negative budget
+    assert r.moe_union_plan_budgeted(ctypes.byref(D), y, y, 8, -1, ctypes.byref(plan), y, None,
+                                     None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_route_plan_budgeted(ctypes.byref(D), y, y, 8, -2, y, y, y, ctypes.byref(plan),
+                                     y, None, y, nb, s0) == lib.MOE_ERR_INVALID_ARG
+    # missing weights or kept-weight output
+    assert r.moe_union_plan_budgeted(ctypes.byref(D), y, None, 8, 4, ctypes.byref(plan), y, None,
+                                     None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_union_plan_budgeted(ctypes.byref(D), y, y, 8, 4, ctypes.byref(plan), None, None,
+                                     None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_route_plan_budgeted(ctypes.byref(D), y, y, 8, 4, y, y, y, ctypes.byref(plan),
+                                     None, None, y, nb, s0) == lib.MOE_ERR_INVALID_ARG
+    # misaligned kept weights; n beyond n_max; a workspace below its header
+    x = P(0x1004)
+    assert r.moe_union_plan_budgeted(ctypes.byref(D), y, y, 8, 4, ctypes.byref(plan), x, None,
+                                     None, s0) == lib.MOE_ERR_ALIGNMENT
+    assert r.moe_union_plan_budgeted(ctypes.byref(D), y, y, 65, 4, ctypes.byref(plan), y, None,
+                                     None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_route_plan_budgeted(ctypes.byref(D), y, y, 8, 4, y, y, y, ctypes.byref(plan),
+                                     y, None, y, 255, s0) == lib.MOE_ERR_WORKSPACE

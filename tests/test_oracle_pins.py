@@ -469,6 +469,10 @@ def test_budget_pass_equals_full_pass_with_dropped_experts_zeroed():
             assert np.array_equal(yb, yz), (gate, B)
             if B >= U:
                 assert np.array_equal(yb, y_full)
+            # a token subset gives the same rows (the kept set still comes from all tokens)
+            sel = [5, 0, 5]
+            _, _, _, ys, keeps = O.verify_budget(L, h, B, tokens=sel, threads=2)
+            assert np.array_equal(keeps, keep) and np.array_equal(ys, yb[sel])
 
 
 def test_budget_zero_leaves_only_the_shared_expert():
