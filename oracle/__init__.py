@@ -83,6 +83,12 @@ def lib():
         L.orc_budget_plan.restype = ctypes.c_int
         L.orc_budget_plan.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       p, p, p, p, p, p, p]
+        L.orc_tree_scores.argtypes = [p, p, ctypes.c_int, p]
+        L.orc_evict_select.restype = ctypes.c_int
+        L.orc_evict_select.argtypes = [p, p, ctypes.c_int, p, p, p, p]
+        L.orc_ecospec_select.restype = ctypes.c_int
+        L.orc_ecospec_select.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, p, ctypes.c_double, p, p]
         L.orc_verify_budget.restype = ctypes.c_int
         L.orc_verify_budget.argtypes = [ctypes.POINTER(_Layer), p, ctypes.c_int, p, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, p, p, p, p, p]
@@ -292,3 +298,55 @@ def verify_budget(layer: Layer, h: np.ndarray, budget: int, tokens=None, threads
     lib().orc_verify_budget(ctypes.byref(c), _ptr(h), n, _ptr(tok), m, threads, budget, _ptr(ids),
                             _ptr(w), _ptr(z), _ptr(y), _ptr(keep))
     return ids, w, z, y, keep.astype(bool)
+
+
+def _tree(parent, q):
+    par = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    qq = np.ascontiguousarray(np.asarray(q, dtype=np.float32))
+    K = par.shape[0]
+    assert qq.shape == (K,) and K >= 1 and par[0] == -1
+    assert all(0 <= par[v] < v for v in range(1, K)), "parent[v] must precede v"
+    return par, qq, K
+
+
+def tree_scores(parent, q) -> np.ndarray:
+    """Cumulative draft score of every node: the product of q along the path
+    from the root (factor 1) to the node ("Making Every Verified Token Count",
+    eq. (7))."""
+    par, qq, K = _tree(parent, q)
+    out = np.zeros(K, dtype=np.float64)
+    lib().orc_tree_scores(_ptr(par), _ptr(qq), K, _ptr(out))
+    return out
+
+
+def evict_select(parent, q, cost):
+    """EVICT's best verification prefix: (k*, order [K], exp_len [K],
+    utility [K]); cost[k-1] = C(k) (float32, widened)."""
+    par, qq, K = _tree(parent, q)
+    c = np.ascontiguousarray(np.asarray(cost, dtype=np.float32))
+    assert c.shape == (K,)
+    order = np.zeros(K, dtype=np.int32)
+    exp_len = np.zeros(K, dtype=np.float64)
+    util = np.zeros(K, dtype=np.float64)
+    ks = lib().orc_evict_select(_ptr(par), _ptr(qq), K, _ptr(c), _ptr(order), _ptr(exp_len),
+                                _ptr(util))
+    return ks, order, exp_len, util
+
+
+def ecospec_select(parent, q, pred_ids, n_experts: int, gamma: int, eps: float, buf0=None):
+    """EcoSpec's cost-aware selection: (selected [min(gamma, K)], buffer
+    [L][E] bool, |buffer|).  pred_ids: [K][L][kp] int32 predicted experts."""
+    par, qq, K = _tree(parent, q)
+    pid = np.ascontiguousarray(np.asarray(pred_ids, dtype=np.int32))
+    assert pid.ndim == 3 and pid.shape[0] == K
+    L, kp = pid.shape[1], pid.shape[2]
+    b0 = None
+    if buf0 is not None:
+        b0 = np.ascontiguousarray(np.asarray(buf0, dtype=np.uint8))
+        assert b0.shape == (L, n_experts)
+    n_sel = min(gamma, K)
+    sel = np.zeros(max(n_sel, 1), dtype=np.int32)
+    buf = np.zeros((L, n_experts), dtype=np.uint8)
+    cnt = lib().orc_ecospec_select(_ptr(par), _ptr(qq), _ptr(pid), K, L, n_experts, kp, gamma,
+                                   _ptr(b0), ctypes.c_double(eps), _ptr(sel), _ptr(buf))
+    return sel[:n_sel].copy(), buf.astype(bool), cnt

@@ -527,3 +527,133 @@ int orc_verify_budget(const orc_layer *L, const void *hs, int n,
   free(ids_l);
   return kept;
 }
+
+/* ----------------------------------------------- pre-verification selection */
+
+/* Draft trees: K nodes, node 0 the root (the token the target model already
+ * sampled), parent[0] = -1 and 0 <= parent[v] < v for every other node.
+ * q[v] is the draft model's probability of node v's token given its prefix. */
+
+/* Cumulative draft score of every node ("Making Every Verified Token Count",
+ * Sec. 3.1, eq. (7)): the product of q over the path from the root to v,
+ * multiplied in path order from the root.  The root's own factor is 1 (a
+ * reading: it is the target's token and is always accepted). */
+void orc_tree_scores(const int32_t *parent, const float *q, int K, double *score) {
+  int32_t *path = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K + 1));
+  for (int v = 0; v < K; ++v) {
+    int len = 0;
+    for (int u = v; u > 0; u = parent[u]) path[len++] = u;  /* v up to a child of the root */
+    double s = 1.0;                                         /* the root */
+    for (int i = len - 1; i >= 0; --i) s *= (double)q[path[i]];
+    score[v] = s;
+  }
+  free(path);
+}
+
+typedef struct {
+  double s;
+  int v;
+} scored_node;
+
+/* larger score first; equal scores, lower node index first (a reading) */
+static int cmp_node(const void *a, const void *b) {
+  const scored_node *x = (const scored_node *)a, *y = (const scored_node *)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->v > y->v) - (x->v < y->v);
+}
+
+/* EVICT's utility-guided prefix ("Making Every Verified Token Count",
+ * Sec. 3.2): T_k = the k nodes of largest score (Sec. 3.2.1);
+ * E_hat[A(T_k)] = the sum of their scores (eq. (8)), added in rank order;
+ * the utility of k is E_hat[A(T_k)] / C(k) (eq. (9) without the constant
+ * C_AR); k* = the k in 1..K of largest utility (eq. (10)), the smallest k on
+ * a tie (a reading).  cost[k-1] = C(k), widened to double.
+ *   order[r]    node of rank r           exp_len[k-1]  E_hat[A(T_k)]
+ *   utility[k-1]                         returns k* */
+int orc_evict_select(const int32_t *parent, const float *q, int K, const float *cost,
+                     int32_t *order, double *exp_len, double *utility) {
+  double *score = (double *)malloc(sizeof(double) * (size_t)K);
+  scored_node *sn = (scored_node *)malloc(sizeof(scored_node) * (size_t)K);
+  orc_tree_scores(parent, q, K, score);
+  for (int v = 0; v < K; ++v) {
+    sn[v].s = score[v];
+    sn[v].v = v;
+  }
+  qsort(sn, (size_t)K, sizeof(scored_node), cmp_node);
+  double acc = 0.0;
+  int best = 1;
+  for (int k = 1; k <= K; ++k) {
+    order[k - 1] = sn[k - 1].v;
+    acc += sn[k - 1].s;
+    exp_len[k - 1] = acc;
+    utility[k - 1] = acc / (double)cost[k - 1];
+    if (utility[k - 1] > utility[best - 1]) best = k;
+  }
+  free(sn);
+  free(score);
+  return best;
+}
+
+/* EcoSpec's cost-aware draft selection ("Less Experts, Faster Decoding",
+ * Sec. 4.2, eqs. (7)-(9), and its appendix algorithm): starting from the
+ * buffer B = B0, gamma times (all K nodes when gamma > K):
+ *   for every unselected node t:  E_traj(t) = the union of the predicted
+ *     expert sets over the path from the root to t (eq. (7));
+ *     cost = |E_traj(t) \ B| (eq. (8));  score = P(t) / (cost + eps) (eq. (9)),
+ *     P(t) the cumulative draft score of orc_tree_scores;
+ *   select the node of largest score (lowest index on a tie: a reading) and
+ *   add E_traj of it to B.
+ * Expert sets are sets of (layer, expert) pairs: pred_ids[v][l][j], j < kp,
+ * names the experts predicted for node v at layer l (ids outside [0, E) are
+ * ignored).  buf0: [L][E] bytes, nonzero = in B0, or NULL for an empty B0.
+ *   selected[i]  the i-th selected node     buf_out  [L][E], the final B
+ * Returns |B| at the end. */
+int orc_ecospec_select(const int32_t *parent, const float *q, const int32_t *pred_ids,
+                       int K, int L, int E, int kp, int gamma, const uint8_t *buf0,
+                       double eps, int32_t *selected, uint8_t *buf_out) {
+  const size_t LE = (size_t)L * (size_t)E;
+  double *P = (double *)malloc(sizeof(double) * (size_t)K);
+  uint8_t *traj = (uint8_t *)calloc((size_t)K * LE, 1);
+  uint8_t *taken = (uint8_t *)calloc((size_t)K, 1);
+  orc_tree_scores(parent, q, K, P);
+  /* eq. (7): walk every node's path and mark the predicted pairs */
+  for (int v = 0; v < K; ++v) {
+    uint8_t *tv = traj + (size_t)v * LE;
+    for (int u = v;; u = parent[u]) {
+      for (int l = 0; l < L; ++l)
+        for (int j = 0; j < kp; ++j) {
+          const int e = pred_ids[((size_t)u * L + l) * kp + j];
+          if (e >= 0 && e < E) tv[(size_t)l * E + e] = 1;
+        }
+      if (u == 0) break;
+    }
+  }
+  for (size_t i = 0; i < LE; ++i) buf_out[i] = buf0 ? (buf0[i] != 0) : 0;
+  const int n_sel = gamma < K ? gamma : K;
+  for (int it = 0; it < n_sel; ++it) {
+    int best = -1;
+    double best_score = 0.0;
+    for (int v = 0; v < K; ++v) {
+      if (taken[v]) continue;
+      const uint8_t *tv = traj + (size_t)v * LE;
+      int cost = 0;
+      for (size_t i = 0; i < LE; ++i) cost += tv[i] && !buf_out[i];
+      const double score = P[v] / ((double)cost + eps);
+      if (best < 0 || score > best_score) {
+        best = v;
+        best_score = score;
+      }
+    }
+    selected[it] = best;
+    taken[best] = 1;
+    const uint8_t *tb = traj + (size_t)best * LE;
+    for (size_t i = 0; i < LE; ++i) buf_out[i] |= tb[i];
+  }
+  int count = 0;
+  for (size_t i = 0; i < LE; ++i) count += buf_out[i];
+  free(taken);
+  free(traj);
+  free(P);
+  return count;
+}

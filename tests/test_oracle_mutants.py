@@ -43,6 +43,22 @@ MUTANTS = {
                                          "if (0 && keep && !keep[ids[j]]) continue;"),
     "budget_dropped_weight_kept": ("w_kept[p] = keep[ids[p]] ? w[p] : 0.0;", "w_kept[p] = w[p];"),
     "budget_plan_counts_dropped": ("if (keep[ids[p]]) hist[ids[p]] += 1;", "hist[ids[p]] += 1;"),
+    "tree_score_skips_own_factor": ("for (int i = len - 1; i >= 0; --i) s *= (double)q[path[i]];",
+                                    "for (int i = len - 1; i >= 1; --i) s *= (double)q[path[i]];"),
+    "evict_ties_to_higher_index": ("return (x->v > y->v) - (x->v < y->v);",
+                                   "return (x->v < y->v) - (x->v > y->v);"),
+    "evict_argmax_last_on_tie": ("if (utility[k - 1] > utility[best - 1]) best = k;",
+                                 "if (utility[k - 1] >= utility[best - 1]) best = k;"),
+    "evict_cost_index_shifted": ("utility[k - 1] = acc / (double)cost[k - 1];",
+                                 "utility[k - 1] = acc / (double)cost[k > 1 ? k - 2 : 0];"),
+    "ecospec_cost_ignores_buffer": ("cost += tv[i] && !buf_out[i];", "cost += tv[i];"),
+    "ecospec_buffer_not_updated": ("for (size_t i = 0; i < LE; ++i) buf_out[i] |= tb[i];",
+                                   "for (size_t i = 0; i < LE; ++i) buf_out[i] |= 0 * tb[i];"),
+    "ecospec_path_without_ancestors": ("      if (u == 0) break;\n    }", "      if (1) break;\n    }"),
+    "ecospec_eps_ignored": ("const double score = P[v] / ((double)cost + eps);",
+                            "const double score = P[v] / ((double)cost + 1.0);"),
+    "ecospec_ties_to_higher_index": ("if (best < 0 || score > best_score) {",
+                                     "if (best < 0 || score >= best_score) {"),
     "budget_plan_not_stable": ("for (int p = 0; p < n_slots; ++p)\n      if (uniq[u] == ids[p])",
                                "for (int p = n_slots - 1; p >= 0; --p)\n      if (uniq[u] == ids[p])"),
 }

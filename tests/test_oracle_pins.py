@@ -508,3 +508,163 @@ def test_budget_e4m3_layer_zeroed_codes():
         lz.w2[torch.from_numpy(~keep)] = 0
         _, _, _, yz = O.verify(oracle_layer(lz), h)
         assert np.array_equal(yb, yz)
+
+
+# ------------------------------------------------ pre-verification selection
+# "Making Every Verified Token Count", Sec. 3 (EVICT) and "Less Experts,
+# Faster Decoding", Sec. 4.2 (EcoSpec).  Trees: node 0 is the root
+# (factor 1), parent[v] < v.
+
+def _random_tree(rng, K, max_children=3):
+    par = [-1]
+    for v in range(1, K):
+        par.append(int(rng.integers(0, v)) if rng.random() < 0.7 else v - 1)
+    return np.array(par, dtype=np.int32)
+
+
+def _ancestor_closed(par, nodes):
+    s = set(int(v) for v in nodes)
+    return all(v == 0 or par[v] in s for v in s)
+
+
+def test_tree_scores_chain_and_log_sum():
+    # a chain with constant acceptance alpha: node i scores alpha^i
+    K, a = 12, 0.75
+    par = np.arange(-1, K - 1, dtype=np.int32)
+    q = np.full(K, a, dtype=np.float32)
+    s = O.tree_scores(par, q)
+    np.testing.assert_allclose(s, [a ** i for i in range(K)], rtol=1e-14)
+    # any tree: the score is exp(sum of log q over the path), the root excluded
+    rng = np.random.default_rng(5)
+    par = _random_tree(rng, 30)
+    q = rng.uniform(0.05, 1.0, 30).astype(np.float32)
+    s = O.tree_scores(par, q)
+    for v in range(30):
+        lg, u = 0.0, v
+        while u > 0:
+            lg += math.log(float(q[u]))
+            u = par[u]
+        assert abs(s[v] - math.exp(lg)) <= 1e-13 * math.exp(lg)
+
+
+def test_evict_chain_closed_forms():
+    # geometric chain: E_hat[A(T_k)] = (1 - a^k) / (1 - a); a constant cost
+    # makes the whole tree best (k* = K); a cost proportional to k makes the
+    # root alone best (k* = 1); C(k) = c0 + c1 k has the closed-form argmax
+    K, a = 16, 0.8
+    par = np.arange(-1, K - 1, dtype=np.int32)
+    q = np.full(K, a, dtype=np.float32)
+    aa = float(np.float32(a))
+    closed = np.array([(1 - aa ** k) / (1 - aa) for k in range(1, K + 1)])
+    ks, order, exp_len, util = O.evict_select(par, q, np.full(K, 3.0))
+    assert ks == K and order.tolist() == list(range(K))
+    np.testing.assert_allclose(exp_len, closed, rtol=1e-13)
+    assert O.evict_select(par, q, 2.5 * np.arange(1, K + 1))[0] == 1
+    for c0, c1 in [(10.0, 1.0), (4.0, 1.0), (1.0, 1.0), (30.0, 0.5)]:
+        f = closed / (c0 + c1 * np.arange(1, K + 1))
+        assert O.evict_select(par, q, c0 + c1 * np.arange(1, K + 1))[0] == int(np.argmax(f)) + 1
+
+
+def test_evict_top_k_is_the_best_subtree_brute_force():
+    # Sec. 3.2.1: the top-k nodes by cumulative score form a valid (ancestor-
+    # closed) subtree whose estimated accepted length is the largest of any
+    # k-node subtree containing the root
+    rng = np.random.default_rng(9)
+    for trial in range(25):
+        K = int(rng.integers(2, 10))
+        par = _random_tree(rng, K)
+        q = rng.uniform(0.05, 1.0, K).astype(np.float32)
+        if trial % 3 == 0:
+            q[:] = 0.5  # ties everywhere
+        s = O.tree_scores(par, q)
+        ks, order, exp_len, util = O.evict_select(par, q, np.ones(K))
+        for k in range(1, K + 1):
+            assert _ancestor_closed(par, order[:k])
+            best = max(sum(s[list(c)]) for c in itertools.combinations(range(K), k)
+                       if 0 in c and _ancestor_closed(par, c))
+            assert abs(exp_len[k - 1] - best) <= 1e-12 * best
+
+
+def test_evict_utility_and_ties():
+    par = np.array([-1, 0, 0, 1, 2], dtype=np.int32)
+    q = np.array([1.0, 0.5, 0.5, 0.5, 0.5], dtype=np.float32)
+    # scores 1, .5, .5, .25, .25: equal scores rank by lower node index
+    ks, order, exp_len, util = O.evict_select(par, q, [1.0, 1.5, 2.0, 2.5, 3.0])
+    assert order.tolist() == [0, 1, 2, 3, 4]
+    assert exp_len.tolist() == [1.0, 1.5, 2.0, 2.25, 2.5]
+    assert util.tolist() == [1.0, 1.0, 1.0, 0.9, 2.5 / 3.0]
+    assert ks == 1  # three-way tie at utility 1: the smallest k
+    # scaling every cost by a constant leaves k* alone
+    rng = np.random.default_rng(10)
+    par = _random_tree(rng, 40)
+    q = rng.uniform(0.1, 1.0, 40).astype(np.float32)
+    cost = 100 + 3.0 * np.arange(1, 41) + rng.uniform(0, 5, 40)
+    assert O.evict_select(par, q, cost)[0] == O.evict_select(par, q, 4.0 * cost)[0]
+
+
+def test_ecospec_hand_worked_example():
+    # root {0,1}; 1 {1,2}; 2 {3,4}; 3 {2,5}; 4 {6,7}; 5 {3,8}; P = 1, .5, .25, .25, .125, .125
+    # step 1: costs 2,3,4,4,5,5 -> node 0;  B = {0,1}
+    # step 2: node 1 costs 1 (.5)                -> node 1;  B = {0,1,2}
+    # step 3: node 2 costs 2 (.125), node 3 costs 1 (.25)   -> node 3;  B += {5}
+    # step 4: node 2 (.125) beats 4 (.0625) and 5 (.125/3)  -> node 2;  B += {3,4}
+    par = [-1, 0, 0, 1, 1, 2]
+    q = [1, .5, .25, .5, .25, .5]
+    pred = np.array([[[0, 1]], [[1, 2]], [[3, 4]], [[2, 5]], [[6, 7]], [[3, 8]]])
+    sel, buf, cnt = O.ecospec_select(par, q, pred, 16, 4, 1e-6)
+    assert sel.tolist() == [0, 1, 3, 2] and cnt == 6
+    assert np.flatnonzero(buf[0]).tolist() == [0, 1, 2, 3, 4, 5]
+    # gamma = 3: confidence order would take node 2 (union 5); EcoSpec takes 3 (union 4)
+    sel, buf, cnt = O.ecospec_select(par, q, pred, 16, 3, 1e-6)
+    assert sel.tolist() == [0, 1, 3] and cnt == 4
+    # eps: a free node wins over a costlier one of larger P when P0/eps > P1/(c+eps)
+    sel, _, _ = O.ecospec_select([-1, 0, 0], [1, .9, .1], np.array([[[0]], [[1]], [[0]]]), 4, 2, 1e-3)
+    assert sel.tolist() == [0, 2]
+    sel, _, _ = O.ecospec_select([-1, 0, 0], [1, .9, .1], np.array([[[0]], [[1]], [[0]]]), 4, 2, 100.0)
+    assert sel.tolist() == [0, 1]
+
+
+def test_ecospec_reduces_to_confidence_order_without_new_experts():
+    # identical predicted sets, or a buffer that already holds every expert:
+    # every cost after the first pick is 0, so the order is by P (ties to
+    # the lower index), the same as EVICT's ranking
+    rng = np.random.default_rng(11)
+    for trial in range(10):
+        K, L, E, kp = 24, 3, 32, 4
+        par = _random_tree(rng, K)
+        q = rng.uniform(0.1, 1.0, K).astype(np.float32)
+        if trial % 2:
+            q[:] = 0.5  # siblings tie: the lower index goes first
+        order = O.evict_select(par, q, np.ones(K))[1]
+        same = np.broadcast_to(rng.integers(0, E, (1, L, kp)), (K, L, kp))
+        for gamma in (1, 5, K, K + 3):
+            sel, buf, cnt = O.ecospec_select(par, q, same, E, gamma, 1e-6)
+            assert sel.tolist() == order[:min(gamma, K)].tolist()
+        pred = rng.integers(0, E, (K, L, kp))
+        full = np.ones((L, E), dtype=np.uint8)
+        sel, buf, cnt = O.ecospec_select(par, q, pred, E, 7, 1e-6, buf0=full)
+        assert sel.tolist() == order[:7].tolist() and cnt == L * E
+
+
+def test_ecospec_selection_is_prefix_closed_and_buffer_is_the_union():
+    # "Less Experts, Faster Decoding", Sec. 4.2 (prefix consistency): a child
+    # never outscores its parent under the same buffer, so the selected set
+    # stays ancestor-closed; the final buffer is B0 plus the predicted sets
+    # of the selected nodes
+    rng = np.random.default_rng(12)
+    for trial in range(20):
+        K, L, E, kp = int(rng.integers(2, 40)), int(rng.integers(1, 4)), 64, 6
+        par = _random_tree(rng, K)
+        q = rng.uniform(0.05, 1.0, K).astype(np.float32)
+        pred = rng.integers(0, E, (K, L, kp))
+        b0 = (rng.random((L, E)) < 0.2).astype(np.uint8)
+        gamma = int(rng.integers(1, K + 2))
+        sel, buf, cnt = O.ecospec_select(par, q, pred, E, gamma, 1e-6, buf0=b0)
+        assert len(set(sel.tolist())) == len(sel) == min(gamma, K)
+        for i in range(1, len(sel) + 1):
+            assert _ancestor_closed(par, sel[:i])
+        want = b0.astype(bool).copy()
+        for v in sel:
+            for l in range(L):
+                want[l, pred[v, l]] = True
+        assert np.array_equal(buf, want) and cnt == want.sum()
