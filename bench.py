@@ -66,6 +66,9 @@ def parse():
     p.add_argument("--budget-config", default=None, choices=sorted(synth.CONFIGS),
                    help="expert-budget sweep (MoE-Spec) on this layer shape, then exit")
     p.add_argument("--budget-n", default="8,16,32,64", help="pass sizes of the budget sweep")
+    p.add_argument("--select-config", default=None, choices=sorted(synth.CONFIGS),
+                   help="EVICT / EcoSpec selection on 64-node trees of this layer, then exit")
+    p.add_argument("--select-trees", type=int, default=64, help="trees in the selection batch")
     p.add_argument("--rho", type=float, default=None, help="chain/tree correlation for the sweep")
     p.add_argument("--sigma", type=float, default=None, help="tree noise for the sweep")
     p.add_argument("--experts", type=int, default=None,
@@ -558,6 +561,139 @@ def run_budget(args):
         "l2": "flushed (2x L2 written then 2x L2 read) before each timed call; median of 5"}))
 
 
+def draft_tree_batch(T, K, seed):
+    """T draft trees of K nodes (the BFS tree shape of the hidden-state
+    recipe) with draft probabilities: each parent's children share one
+    Dirichlet(0.5) draw over (children + the rest of the vocabulary)."""
+    import numpy as np
+    par = np.array(synth.tree_parents(K), dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    q = np.ones((T, K), dtype=np.float32)
+    kids = {}
+    for v in range(1, K):
+        kids.setdefault(int(par[v]), []).append(v)
+    for t in range(T):
+        for p_, ch in kids.items():
+            d = rng.dirichlet(np.full(len(ch) + 1, 0.5))
+            q[t, ch] = np.sort(d[:-1])[::-1]  # the draft ranks its children by probability
+    return np.broadcast_to(par, (T, K)).copy(), q
+
+
+def run_select(args):
+    """--select-config NAME: pre-verification selection on a batch of
+    --select-trees draft trees of 64 nodes.
+
+    - EVICT (utility-guided prefix): C(k) is this library's measured layer
+      pass (route + plan + dedup) at n = k. It reports k* over the trees and
+      the kernel's µs for the batch (20 calls in one CUDA graph).
+    - EcoSpec (cost-aware selection), at gamma = 4, 8, 16, with the layer's
+      own routing as the predicted sets (a perfect predictor). It reports the
+      kernel's µs, the mean union of the selected nodes against the
+      confidence-ranked top-gamma, and the measured verify pass of both node
+      sets (L2 flushed, median of 3)."""
+    import numpy as np
+    from moe_expert_ffn_gemv_gb300 import binding as mv
+    torch.cuda.set_device(0)
+    cfg = synth.CONFIGS[args.select_config]
+    layer = synth.make_layer(cfg, seed=1, device="cuda")
+    K, T = 64, args.select_trees
+    par, q = draft_tree_batch(T, K, seed=11)
+    vl = mv.VerifyLayer(layer, K)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    fa = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    fb = torch.ones_like(fa)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps=3, flush=True):
+        ts = []
+        for _ in range(reps):
+            if flush:
+                flush_l2(fa, fb)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    def verify_pass(h):
+        n = h.shape[0]
+        vl.route_plan(h, n)
+        vl.dedup(h, n)
+
+    hs = [synth.make_hidden(cfg, K, seed=100 + t, device="cuda") for t in range(T)]
+    ids = []
+    for h in hs:
+        vl.route(h, K)
+        ids.append(vl.ids_view(K).clone())
+    ids = torch.stack(ids)                               # [T][K][k]
+    # EVICT: C(k) from the measured pass on tree 0's first k nodes
+    cost = np.array([timed(lambda: verify_pass(hs[0][:k].contiguous())) * 1e6
+                     for k in range(1, K + 1)], dtype=np.float32)
+    par_d = torch.from_numpy(par).cuda()
+    q_d = torch.from_numpy(q).cuda()
+    cost_d = torch.from_numpy(cost).cuda()
+
+    def graph_us(call, reps=20):
+        """µs per call: `reps` calls on preallocated buffers captured in one
+        CUDA graph, so that host latency stays out of the device time."""
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        return 1e6 * timed(g.replay, reps=5, flush=False) / reps
+
+    ev_out = [torch.empty(T, K, dtype=torch.int32, device="cuda"),
+              torch.empty(T, K, dtype=torch.float64, device="cuda"),
+              torch.empty(T, K, dtype=torch.float64, device="cuda"),
+              torch.empty(T, dtype=torch.int32, device="cuda")]
+    out = {}
+    t_ev = graph_us(lambda: mv.moe_evict_select(par_d, q_d, T, K, cost_d, *ev_out))
+    k_star = mv.evict_select(par_d, q_d, cost_d)[0].cpu().numpy()
+    out["evict"] = {"kernel_us_batch": round(t_ev, 2),
+                    "k_star": {"min": int(k_star.min()), "median": float(np.median(k_star)),
+                               "max": int(k_star.max())},
+                    "cost_us_at_k": {str(k): round(float(cost[k - 1]), 1)
+                                     for k in (1, 2, 4, 8, 16, 32, 64)}}
+    order = mv.evict_select(par_d, q_d, cost_d)[1].cpu().numpy()
+    pred = ids[:, :, None, :].contiguous()
+    eco = []
+    n_meas = min(T, 16)
+    for gamma in (4, 8, 16):
+        eco_out = [torch.empty(T, gamma, dtype=torch.int32, device="cuda"),
+                   torch.empty(T, 1, (cfg.n_experts + 31) // 32, dtype=torch.int32, device="cuda"),
+                   torch.empty(T, dtype=torch.int32, device="cuda")]
+        t_k = graph_us(lambda: mv.moe_ecospec_select(par_d, q_d, pred, T, K, 1, cfg.n_experts,
+                                                     cfg.top_k, gamma, 1e-6, None, *eco_out))
+        sel, _, usz = mv.ecospec_select(par_d, q_d, pred, cfg.n_experts, gamma, 1e-6)
+        sel = sel.cpu().numpy()
+        ids_np = ids.cpu().numpy()
+        u_eco = [len(set(ids_np[t][sel[t]].ravel().tolist())) for t in range(T)]
+        u_conf = [len(set(ids_np[t][order[t, :gamma]].ravel().tolist())) for t in range(T)]
+        assert u_eco == usz.cpu().tolist()
+        t_eco = [timed(lambda: verify_pass(hs[t][torch.from_numpy(sel[t]).long().cuda()]
+                                           .contiguous())) for t in range(n_meas)]
+        t_conf = [timed(lambda: verify_pass(hs[t][torch.from_numpy(order[t, :gamma].copy())
+                                                  .long().cuda()].contiguous()))
+                  for t in range(n_meas)]
+        eco.append({"gamma": gamma, "kernel_us_batch": round(t_k, 2),
+                    "U_ecospec_mean": round(float(np.mean(u_eco)), 2),
+                    "U_confidence_mean": round(float(np.mean(u_conf)), 2),
+                    "us_verify_ecospec": round(1e6 * float(np.mean(t_eco)), 1),
+                    "us_verify_confidence": round(1e6 * float(np.mean(t_conf)), 1),
+                    "trees_timed": n_meas})
+    out["ecospec"] = eco
+    assert vl.last_error() == 0
+    print(json.dumps({"select_config": cfg.name, "trees": T, "nodes": K,
+                      "hidden": cfg.hidden, **out}))
+
+
 # ------------------------------------------------------------- cpu / oracle
 
 def oracle_inputs(layer, h):
@@ -644,6 +780,8 @@ def main():
         run_fit(args)
     elif args.budget_config:
         run_budget(args)
+    elif args.select_config:
+        run_select(args)
     elif args.sweep_config:
         run_sweep_only(args)
     elif args.impl == "reference":

@@ -275,6 +275,70 @@ moe_status moe_verify_perslot(const moe_layer_desc *desc,
                               const float *w, void *workspace, size_t ws_bytes,
                               void *y, moe_stream_t stream);
 
+/* ---- pre-verification selection over a batch of draft trees ----
+ *
+ * Before the verification pass, these calls choose which draft-tree nodes
+ * to verify.  Each tree has K = n_nodes nodes:
+ *   parent  device [n_trees][K] int32: node 0 is the root (the token the
+ *           target model already sampled), parent[0] = -1, and
+ *           0 <= parent[v] < v for every other node (e.g. BFS numbering);
+ *   q       device [n_trees][K] float: the draft model's probability of node
+ *           v's token given its prefix (q of the root is not read: the root
+ *           counts with factor 1).
+ * A node's cumulative score is the product of q along its root path
+ * ("Making Every Verified Token Count", Sec. 3.1, eq. (7)).  Both calls
+ * decide in double, in the order the definitions give, so their outputs are
+ * exact.  Ties go to the lower node index (or the smaller k).  A malformed
+ * tree makes moe_last_error() report MOE_ERR_DEVICE_INPUT (through
+ * error_word, when not NULL), and that tree's outputs are marked
+ * (k_star 0 / selected -1 / union_size -1).  1 <= K <= 256; n_trees == 0
+ * enqueues nothing. */
+
+/* EVICT's utility-guided prefix ("Making Every Verified Token Count",
+ * Sec. 3.2): T_k = the k nodes of largest score (an ancestor-closed subtree,
+ * Sec. 3.2.1); E_hat[A(T_k)] = the sum of their scores (eq. (8)), added in
+ * rank order; k* = argmax over k = 1..K of E_hat[A(T_k)] / C(k) (eqs. (9)-
+ * (10)), with C(k) a profiled cost table (Sec. 3.2.3).
+ *   cost      device [K] float: C(k) at cost[k-1], shared by all trees
+ *   order     device [n_trees][K] int32 (out): nodes by rank; verify the
+ *             first k_star of them
+ *   exp_len   device [n_trees][K] double (out, or NULL): E_hat[A(T_k)]
+ *   utility   device [n_trees][K] double (out, or NULL): E_hat / C(k)
+ *   k_star    device [n_trees] int32 (out) */
+moe_status moe_evict_select(const int32_t *parent, const float *q,
+                            int32_t n_trees, int32_t n_nodes, const float *cost,
+                            int32_t *order, double *exp_len, double *utility,
+                            int32_t *k_star, int32_t *error_word,
+                            moe_stream_t stream);
+
+/* EcoSpec's cost-aware draft selection ("Less Experts, Faster Decoding:
+ * Cost-Aware Speculative Decoding for Mixture-of-Experts", Sec. 4.2,
+ * eqs. (7)-(9), and its appendix algorithm).  Start from the buffer B = B0,
+ * then repeat gamma times (K times when gamma > K):
+ *   - for every unselected node t, E_traj(t) is the union of the predicted
+ *     (layer, expert) sets over t's root path;
+ *   - its score is P(t) / (|E_traj(t) \ B| + eps);
+ *   - select the node of largest score and add its E_traj to B.
+ *   pred_ids    device [n_trees][K][n_layers][pred_k] int32: the experts
+ *               predicted for each node at each layer (ids outside
+ *               [0, n_experts) are ignored)
+ *   eps         > 0
+ *   buffer0     device [n_trees][n_layers][ceil(n_experts/32)] uint32
+ *               bitsets (bit e%32 of word e/32) of B0, or NULL for empty
+ *   selected    device [n_trees][min(gamma, K)] int32 (out), in pick order
+ *   buffer_out  device, the final B in buffer0's layout (out, or NULL)
+ *   union_size  device [n_trees] int32 (out): |B| at the end
+ * MOE_ERR_UNSUPPORTED when (K + 1) * n_layers * ceil(n_experts/32) * 4
+ * bytes exceed 200 KB (the bitsets live in shared memory). */
+moe_status moe_ecospec_select(const int32_t *parent, const float *q,
+                              const int32_t *pred_ids, int32_t n_trees,
+                              int32_t n_nodes, int32_t n_layers,
+                              int32_t n_experts, int32_t pred_k, int32_t gamma,
+                              double eps, const uint32_t *buffer0,
+                              int32_t *selected, uint32_t *buffer_out,
+                              int32_t *union_size, int32_t *error_word,
+                              moe_stream_t stream);
+
 /* Zeroes the error word at the start of a fresh workspace (enqueued on
  * `stream`).  Call once after allocating a workspace; moe_last_error() clears
  * the word again after reading it. */

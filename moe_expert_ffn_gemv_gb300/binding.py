@@ -35,7 +35,8 @@ EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_to
             "moe_union_plan", "moe_verify_dedup", "moe_verify_perslot", "moe_workspace_init",
             "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
             "moe_pack_expert_weights", "moe_verify_dedup_noalloc", "moe_route_plan",
-            "moe_union_plan_budgeted", "moe_route_plan_budgeted"]
+            "moe_union_plan_budgeted", "moe_route_plan_budgeted", "moe_evict_select",
+            "moe_ecospec_select"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -76,6 +77,13 @@ _lib.moe_route_plan_budgeted.restype = ctypes.c_int
 _lib.moe_route_plan_budgeted.argtypes = [_D, _P, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P,
                                          ctypes.POINTER(moe_plan), _P, _P, _P, ctypes.c_size_t,
                                          _P]
+_lib.moe_evict_select.restype = ctypes.c_int
+_lib.moe_evict_select.argtypes = [_P, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
+                                  _P]
+_lib.moe_ecospec_select.restype = ctypes.c_int
+_lib.moe_ecospec_select.argtypes = [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_double, _P, _P, _P, _P, _P, _P]
 _lib.moe_verify_dedup.restype = ctypes.c_int
 _lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32, _P,
                                   _P, ctypes.POINTER(moe_plan), _P, ctypes.c_size_t, _P, _P]
@@ -174,6 +182,23 @@ def moe_route_plan_budgeted(desc, router_w, h, n, budget, ids, w, logits, plan: 
                                         _ptr(w_kept), _ptr(routed_union), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "moe_route_plan_budgeted")
+
+
+def moe_evict_select(parent, q, n_trees, n_nodes, cost, order, exp_len, utility, k_star,
+                     error_word=None, stream=None) -> None:
+    _check(_lib.moe_evict_select(_ptr(parent), _ptr(q), n_trees, n_nodes, _ptr(cost), _ptr(order),
+                                 _ptr(exp_len), _ptr(utility), _ptr(k_star), _ptr(error_word),
+                                 _stream(stream)), "moe_evict_select")
+
+
+def moe_ecospec_select(parent, q, pred_ids, n_trees, n_nodes, n_layers, n_experts, pred_k, gamma,
+                       eps, buffer0, selected, buffer_out, union_size, error_word=None,
+                       stream=None) -> None:
+    _check(_lib.moe_ecospec_select(_ptr(parent), _ptr(q), _ptr(pred_ids), n_trees, n_nodes,
+                                   n_layers, n_experts, pred_k, gamma, ctypes.c_double(eps),
+                                   _ptr(buffer0), _ptr(selected), _ptr(buffer_out),
+                                   _ptr(union_size), _ptr(error_word), _stream(stream)),
+           "moe_ecospec_select")
 
 
 def moe_verify_dedup(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_plan, workspace,
@@ -405,3 +430,47 @@ class VerifyLayer:
 
     def logits_view(self, n):
         return self.logits[:n * self.cfg.n_experts].view(n, self.cfg.n_experts)
+
+
+# -------------------------------------------------- pre-verification selection
+
+def _i32(x, device):
+    return torch.as_tensor(x, dtype=torch.int32).contiguous().to(device)
+
+
+def evict_select(parent, q, cost, error_word=None):
+    """EVICT's best prefix for a batch of trees on the GPU.  parent, q:
+    [trees][K] (int32 / float32 tensors or arrays, moved to the GPU); cost:
+    [K] C(k).  Returns (k_star [trees], order [trees][K], exp_len, utility)
+    as device tensors."""
+    parent = _i32(parent, "cuda")
+    q = torch.as_tensor(q, dtype=torch.float32).contiguous().cuda()
+    cost = torch.as_tensor(cost, dtype=torch.float32).contiguous().cuda()
+    T, K = parent.shape
+    order = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    exp_len = torch.empty(T, K, dtype=torch.float64, device="cuda")
+    util = torch.empty(T, K, dtype=torch.float64, device="cuda")
+    k_star = torch.empty(max(T, 1), dtype=torch.int32, device="cuda")
+    moe_evict_select(parent, q, T, K, cost, order, exp_len, util, k_star, error_word)
+    return k_star[:T], order, exp_len, util
+
+
+def ecospec_select(parent, q, pred_ids, n_experts: int, gamma: int, eps: float, buffer0=None,
+                   error_word=None):
+    """EcoSpec's cost-aware selection for a batch of trees on the GPU.
+    pred_ids: [trees][K][L][kp]; buffer0: [trees][L][ceil(E/32)] uint32 bit
+    words (as int32) or None.  Returns (selected [trees][min(gamma,K)],
+    buffer [trees][L][words] (int32 view of the bits), union_size [trees])."""
+    parent = _i32(parent, "cuda")
+    q = torch.as_tensor(q, dtype=torch.float32).contiguous().cuda()
+    pred = _i32(pred_ids, "cuda")
+    T, K, L, kp = pred.shape
+    wpl = (n_experts + 31) // 32
+    n_sel = min(gamma, K)
+    sel = torch.empty(T, max(n_sel, 1), dtype=torch.int32, device="cuda")
+    buf = torch.empty(T, L, wpl, dtype=torch.int32, device="cuda")
+    usz = torch.empty(max(T, 1), dtype=torch.int32, device="cuda")
+    b0 = None if buffer0 is None else _i32(buffer0, "cuda")
+    moe_ecospec_select(parent, q, pred, T, K, L, n_experts, kp, gamma, eps, b0, sel, buf, usz,
+                       error_word)
+    return sel[:, :n_sel], buf, usz[:T]

@@ -375,6 +375,46 @@ MOE_API moe_status moe_route_plan_budgeted(const moe_layer_desc *desc, const voi
                     workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+MOE_API moe_status moe_evict_select(const int32_t *parent, const float *q, int32_t n_trees,
+                                    int32_t n_nodes, const float *cost, int32_t *order,
+                                    double *exp_len, double *utility, int32_t *k_star,
+                                    int32_t *error_word, moe_stream_t stream) {
+  if (n_trees < 0 || n_nodes < 1 || n_nodes > SEL_MAX_NODES) return MOE_ERR_INVALID_ARG;
+  if (n_trees == 0) return MOE_OK;
+  if (!parent || !q || !cost || !order || !k_star) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(parent) || !aligned16(q) || !aligned16(cost) || !aligned16(order) ||
+      !aligned16(k_star) || (exp_len && !aligned16(exp_len)) ||
+      (utility && !aligned16(utility)))
+    return MOE_ERR_ALIGNMENT;
+  return cuda_status(launch_evict_select(parent, q, n_trees, n_nodes, cost, order, exp_len,
+                                         utility, k_star, error_word,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+MOE_API moe_status moe_ecospec_select(const int32_t *parent, const float *q,
+                                      const int32_t *pred_ids, int32_t n_trees, int32_t n_nodes,
+                                      int32_t n_layers, int32_t n_experts, int32_t pred_k,
+                                      int32_t gamma, double eps, const uint32_t *buffer0,
+                                      int32_t *selected, uint32_t *buffer_out,
+                                      int32_t *union_size, int32_t *error_word,
+                                      moe_stream_t stream) {
+  if (n_trees < 0 || n_nodes < 1 || n_nodes > SEL_MAX_NODES || n_layers < 1 || n_experts < 1 ||
+      pred_k < 1 || gamma < 0 || !(eps > 0.0))
+    return MOE_ERR_INVALID_ARG;
+  if (ecospec_smem_bytes(n_nodes, n_layers, n_experts) > SEL_MAX_SMEM) return MOE_ERR_UNSUPPORTED;
+  if (n_trees == 0) return MOE_OK;
+  if (!parent || !q || !pred_ids || !union_size || (gamma > 0 && !selected))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(parent) || !aligned16(q) || !aligned16(pred_ids) || !aligned16(union_size) ||
+      (selected && !aligned16(selected)) || (buffer0 && !aligned16(buffer0)) ||
+      (buffer_out && !aligned16(buffer_out)))
+    return MOE_ERR_ALIGNMENT;
+  return cuda_status(launch_ecospec_select(parent, q, pred_ids, n_trees, n_nodes, n_layers,
+                                           n_experts, pred_k, gamma, eps, buffer0, selected,
+                                           buffer_out, union_size, error_word,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 MOE_API moe_status moe_verify_dedup(const moe_layer_desc *desc, const moe_expert_weights *weights,
                                     const void *h, int32_t n, const int32_t *ids, const float *w,
                                     const moe_plan *plan, void *workspace, size_t ws_bytes,

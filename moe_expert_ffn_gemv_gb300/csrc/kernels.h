@@ -82,6 +82,21 @@ cudaError_t launch_union_plan_budgeted(const int32_t *ids, const float *w, int n
                                        float *w_kept, int32_t *routed_u, int32_t *err,
                                        cudaStream_t stream);
 
+// Pre-verification selection over a batch of draft trees (select.cu), one
+// CTA per tree of at most SEL_MAX_NODES nodes.
+constexpr int SEL_MAX_NODES = 256;
+constexpr size_t SEL_MAX_SMEM = 200 * 1024;  // EcoSpec bitsets: (K + 1) words x layers x E/32
+cudaError_t launch_evict_select(const int32_t *parent, const float *q, int n_trees, int K,
+                                const float *cost, int32_t *order, double *exp_len,
+                                double *utility, int32_t *k_star, int32_t *err,
+                                cudaStream_t stream);
+size_t ecospec_smem_bytes(int K, int n_layers, int n_experts);
+cudaError_t launch_ecospec_select(const int32_t *parent, const float *q, const int32_t *pred,
+                                  int n_trees, int K, int n_layers, int n_experts, int kp,
+                                  int gamma, double eps, const uint32_t *buf0,
+                                  int32_t *selected, uint32_t *buf_out, int32_t *union_size,
+                                  int32_t *err, cudaStream_t stream);
+
 // y[t] = sum_j w[t][j] yslot[t*k+j] (+ yslot[n*k+t]) -> y (fp32 or bf16).
 cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,
                            bool out_bf16, void *y, cudaStream_t stream);

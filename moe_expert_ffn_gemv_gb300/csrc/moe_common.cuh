@@ -25,6 +25,16 @@ __device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// An unsigned integer with the order of the double s (for s not NaN): the
+// sign bit flipped for s >= 0, all bits flipped for s < 0, and -0 taken as
+// +0 so that equal values give equal keys.  Every key of a non-NaN value is
+// above 0.  Ranking on keys costs integer compares instead of fp64 ones.
+__device__ __forceinline__ unsigned long long order_key(double s) {
+  if (s == 0.0) s = 0.0;
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(s));
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -161,16 +161,6 @@ __device__ __forceinline__ ExpertScan plan_scan(PlanSmem &S, int n_experts) {
   return x;
 }
 
-// An unsigned integer with the order of the double s (for s not NaN): the
-// sign bit flipped for s >= 0, all bits flipped for s < 0, and -0 taken as
-// +0 so that equal contributions give equal keys.  Ranking on the key costs
-// integer compares instead of fp64 ones.
-__device__ __forceinline__ unsigned long long order_key(double s) {
-  if (s == 0.0) s = 0.0;
-  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(s));
-  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
-}
-
 // (key a, expert e) ranks before (key b, expert f): larger contribution, or
 // equal and lower id.
 __device__ __forceinline__ bool budget_beats(unsigned long long a, int e, unsigned long long b,

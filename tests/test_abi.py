@@ -145,3 +145,29 @@ def test_budgeted_plan_calls_reject_bad_arguments_before_any_launch(lib):
                                      None, s0) == lib.MOE_ERR_INVALID_ARG
     assert r.moe_route_plan_budgeted(ctypes.byref(D), y, y, 8, 4, y, y, y, ctypes.byref(plan),
                                      y, None, y, 255, s0) == lib.MOE_ERR_WORKSPACE
+
+
+def test_selection_calls_reject_bad_arguments_before_any_launch(lib):
+    P = ctypes.c_void_p
+    r = lib._lib
+    s0 = P(0)
+    y = P(0x1000)
+    x = P(0x1004)
+    # EVICT: node count out of range, missing outputs, misaligned arrays; no trees is a no-op
+    assert r.moe_evict_select(y, y, 2, 0, y, y, None, None, y, None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_evict_select(y, y, 2, 257, y, y, None, None, y, None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_evict_select(y, y, 2, 8, y, None, None, None, y, None, s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_evict_select(y, x, 2, 8, y, y, None, None, y, None, s0) == lib.MOE_ERR_ALIGNMENT
+    assert r.moe_evict_select(None, None, 0, 8, None, None, None, None, None, None, s0) == lib.MOE_OK
+    # EcoSpec: eps must be positive; gamma >= 0; bitsets beyond shared memory are unsupported
+    eco = lambda *a: r.moe_ecospec_select(*a)
+    assert eco(y, y, y, 1, 8, 1, 64, 4, 2, ctypes.c_double(0.0), None, y, None, y, None,
+               s0) == lib.MOE_ERR_INVALID_ARG
+    assert eco(y, y, y, 1, 8, 1, 64, 4, -1, ctypes.c_double(1e-6), None, y, None, y, None,
+               s0) == lib.MOE_ERR_INVALID_ARG
+    assert eco(y, y, y, 1, 256, 64, 256, 8, 4, ctypes.c_double(1e-6), None, y, None, y, None,
+               s0) == lib.MOE_ERR_UNSUPPORTED
+    assert eco(y, y, None, 1, 8, 1, 64, 4, 2, ctypes.c_double(1e-6), None, y, None, y, None,
+               s0) == lib.MOE_ERR_INVALID_ARG
+    assert eco(y, y, y, 1, 8, 1, 64, 4, 2, ctypes.c_double(1e-6), x, y, None, y, None,
+               s0) == lib.MOE_ERR_ALIGNMENT
