@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const float *_
                                                                   int n, int k, int d,
                                                                   int n_shared,
                                                                   void *__restrict__ y) {
+  pdl_wait();  // the expert kernel's rows (launched as its programmatic dependent)
   const int t = blockIdx.y;
   const int c = (blockIdx.x * COMBINE_THREADS + threadIdx.x) * 4;
   if (c >= d) return;
@@ -78,10 +79,10 @@ cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int
                            bool out_bf16, void *y, cudaStream_t stream) {
   dim3 grid((d / 4 + COMBINE_THREADS - 1) / COMBINE_THREADS, n);
   if (out_bf16)
-    combine_kernel<true><<<grid, COMBINE_THREADS, 0, stream>>>(yslot, w, n, k, d, n_shared, y);
-  else
-    combine_kernel<false><<<grid, COMBINE_THREADS, 0, stream>>>(yslot, w, n, k, d, n_shared, y);
-  return cudaGetLastError();
+    return launch_dependent(combine_kernel<true>, grid, dim3(COMBINE_THREADS), 0, stream, yslot,
+                            w, n, k, d, n_shared, y);
+  return launch_dependent(combine_kernel<false>, grid, dim3(COMBINE_THREADS), 0, stream, yslot, w,
+                          n, k, d, n_shared, y);
 }
 
 }  // namespace moe

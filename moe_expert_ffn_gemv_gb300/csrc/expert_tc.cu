@@ -190,6 +190,15 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = P.T.n * P.T.k;
+  // Launch order: the plan, phase 1, phase 2, the combine, each of the last
+  // three launched as a programmatic dependent of the one before.  Phase 1
+  // reads the plan at once, so it waits first; it triggers only after that
+  // wait, so phase 2 never starts before the plan is complete.  Phase 2
+  // reads phase 1's activations only in its consumer warps, which wait
+  // there; its producer streams weights from the start, behind the end of
+  // phase 1.
+  if (PHASE == 1) pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -338,6 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   }
 
   // -------------------------------------------------------------- consumers
+  if (PHASE == 2) pdl_wait();  // phase 1's activations
   const int g = lane >> 2, c = lane & 3;
   const int tid = threadIdx.x;
   const uint16_t *act = static_cast<const uint16_t *>(P.act);
@@ -571,8 +581,7 @@ cudaError_t launch_one(const TcParams &P, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  kern<<<grid, THREADS, smem, stream>>>(P);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(THREADS), smem, stream, P);
 }
 
 template <bool FP8, int PHASE>

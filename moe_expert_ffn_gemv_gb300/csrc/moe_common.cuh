@@ -35,6 +35,17 @@ __device__ __forceinline__ unsigned long long order_key(double s) {
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start before the kernel ahead of it in
+// the stream has finished: pdl_wait() returns once that kernel has completed
+// and its memory is visible (at once when the launch had no such
+// attribute), and pdl_trigger() lets the kernel behind this one start
+// launching once every CTA of this one has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) union_plan_kernel(
     int64_t expert_bytes, int budget, int32_t *hist, int32_t *uniq, int32_t *n_uniq,
     int32_t *offs, int32_t *perm, int64_t *union_bytes, float *w_kept, int32_t *routed_u,
     int32_t *err) {
+  pdl_trigger();  // the expert kernel behind this one may launch (it waits for the plan)
   __shared__ PlanSmem S;
   if constexpr (BUDGET) {
     __shared__ BudgetSmem B;

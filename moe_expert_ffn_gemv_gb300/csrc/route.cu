@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
     int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
     int64_t *union_bytes, int budget, float *w_kept, int32_t *routed_u, int32_t *err,
     unsigned int *counter) {
+  pdl_trigger();  // the expert kernel behind this one may launch (it waits for the plan)
   router_scores_cta(wg, h, n, d, n_experts, logits);
   __shared__ int s_last;
   __syncthreads();
