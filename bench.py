@@ -69,6 +69,12 @@ def parse():
     p.add_argument("--select-config", default=None, choices=sorted(synth.CONFIGS),
                    help="EVICT / EcoSpec selection on 64-node trees of this layer, then exit")
     p.add_argument("--select-trees", type=int, default=64, help="trees in the selection batch")
+    p.add_argument("--stack-config", default=None, choices=sorted(synth.CONFIGS),
+                   help="multi-layer pass and best draft length on this layer shape, then exit")
+    p.add_argument("--layers", type=int, default=8, help="MoE layers of the stack")
+    p.add_argument("--max-drafts", type=int, default=15, help="largest K (n = K + 1 tokens)")
+    p.add_argument("--t-draft", type=float, default=0.0,
+                   help="draft cost of one position in µs (added as K * t_draft)")
     p.add_argument("--rho", type=float, default=None, help="chain/tree correlation for the sweep")
     p.add_argument("--sigma", type=float, default=None, help="tree noise for the sweep")
     p.add_argument("--experts", type=int, default=None,
@@ -694,6 +700,94 @@ def run_select(args):
                       "hidden": cfg.hidden, **out}))
 
 
+def run_stack(args):
+    """--stack-config NAME --layers L: the verify pass of L MoE layers (one
+    CUDA graph per pass size) for K = 0..--max-drafts drafts (n = K + 1
+    tokens of a chain or tree, the layer's recipe), over --windows hidden-
+    state windows.  Reports per K the median stack time T_T(K) and the
+    layer-averaged union U_bar ("The Limits of Speculation", eq. (5)); the
+    cost model T_T = beta0(m) + alpha(m) U_bar per m (its eq. (4), no
+    context term) and pooled over m (eq. (3)); and, with the step time
+    V(K) = T_T(K) + K * --t-draft, the best draft length k*(a) under
+    geometric acceptance, its staircase, a0 and the speedup
+    ("Speculative Decoding for MoE Models: Expert Bytes, ...").  The
+    calibrated step time (the pooled fit at each K's mean U_bar) gives
+    k_hat*(a); its relative error delta feeds bound (20)."""
+    import numpy as np
+    from moe_expert_ffn_gemv_gb300 import binding as mv
+    from moe_expert_ffn_gemv_gb300 import draft_length as D
+    torch.cuda.set_device(0)
+    cfg = synth.CONFIGS[args.stack_config]
+    L, Kmax, W = args.layers, args.max_drafts, args.windows
+    n_max = Kmax + 1
+    st = mv.VerifyStack.synthetic(cfg, L, n_max, seed=1)
+    hs = torch.empty(L, n_max, cfg.d, dtype=synth.torch_dtype(cfg.act), device="cuda")
+    windows = [torch.stack([synth.make_hidden(cfg, n_max, seed=5000 + 100 * w + l, device="cuda",
+                                              rho=args.rho, sigma=args.sigma)
+                            for l in range(L)]) for w in range(W)]
+    stream = torch.cuda.current_stream()
+    rounds = []
+    for K in range(Kmax + 1):
+        n = K + 1
+        hs.copy_(windows[0])
+        g = st.capture(hs, n)
+        for w in range(W):
+            hs.copy_(windows[w])
+            g.replay()  # warm
+            ts = []
+            for _ in range(3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            rounds.append({"K": K, "m": n, "w": w, "t": statistics.median(ts),
+                           "u_bar": D.layer_mean_union(st.unions())})
+        del g
+    assert st.last_error() == 0
+    t_med = [statistics.median(r["t"] for r in rounds if r["K"] == K) for K in range(Kmax + 1)]
+    u_mean = [statistics.mean(r["u_bar"] for r in rounds if r["K"] == K) for K in range(Kmax + 1)]
+    per_m = D.fit_cost_model(rounds)
+    pooled = D.fit_cost_model([dict(r, m=0) for r in rounds])[0]
+    V = D.step_time(t_med, args.t_draft)
+    V_hat = D.step_time([pooled["beta0"] + pooled["alpha"] * u for u in u_mean], args.t_draft)
+    delta = max(abs(vh / v - 1) for vh, v in zip(V_hat, V))
+    grid = [i / 100 for i in range(0, 100)]
+    agree = sum(D.best_draft_length(a, V_hat) == D.best_draft_length(a, V) for a in grid)
+    inside = sum(D.throughput(a, V, D.best_draft_length(a, V_hat))
+                 >= D.bound_best_length(delta) * D.throughput(a, V, D.best_draft_length(a, V))
+                 for a in grid)
+    at = {}
+    for a in (0.5, 0.6, 0.7, 0.8, 0.9):
+        k = D.best_draft_length(a, V)
+        at[str(a)] = {"k_star": k, "speedup": round(D.speedup(a, V, k), 3),
+                      "moesd_speedup": round(D.moesd_speedup(D.expected_tokens(a, k), k,
+                                                             args.t_draft, t_med), 3)}
+    print(json.dumps({
+        "stack_config": cfg.name, "layers": L, "windows": W, "t_draft_us": args.t_draft,
+        "hidden": cfg.hidden, "rho": args.rho if args.rho is not None else cfg.rho,
+        "sigma": args.sigma if args.sigma is not None else cfg.sigma,
+        "per_K": [{"K": K, "us_stack": round(t_med[K], 1), "u_bar": round(u_mean[K], 2),
+                   "us_per_layer": round(t_med[K] / L, 1)} for K in range(Kmax + 1)],
+        "cost_model_per_m": {str(m): {"alpha_us": round(f["alpha"], 3),
+                                      "beta0_us": round(f["beta0"], 1),
+                                      "r2": None if f["r2"] != f["r2"] else round(f["r2"], 3)}
+                             for m, f in per_m.items()},
+        "cost_model_pooled": {"alpha_us": round(pooled["alpha"], 3),
+                              "beta0_us": round(pooled["beta0"], 1),
+                              "r2": round(pooled["r2"], 4)},
+        "a0": round(D.a0(V), 4),
+        "staircase": [[round(a_, 4), k] for a_, k in D.staircase(V)],
+        "best_at": at,
+        "calibrated": {"delta": round(delta, 4),
+                       "k_star_agrees": f"{agree} of {len(grid)} acceptance values",
+                       "inside_bound_20": f"{inside} of {len(grid)}"},
+        "timing": "graph replay of the whole stack, median of 3 after one warm replay; the "
+                  "stack's expert bytes exceed L2"}))
+
+
 # ------------------------------------------------------------- cpu / oracle
 
 def oracle_inputs(layer, h):
@@ -782,6 +876,8 @@ def main():
         run_budget(args)
     elif args.select_config:
         run_select(args)
+    elif args.stack_config:
+        run_stack(args)
     elif args.sweep_config:
         run_sweep_only(args)
     elif args.impl == "reference":

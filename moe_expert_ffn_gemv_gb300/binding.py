@@ -421,6 +421,14 @@ class VerifyLayer:
     def last_error(self) -> int:
         return moe_last_error(self.workspace)
 
+    def release_unpacked(self) -> None:
+        """Drop this object's references to the row-major expert weights
+        (the packed copy is what the kernels read); the router weights and
+        the scale tables stay."""
+        L = self.layer
+        self.layer = synth.Layer(L.cfg, L.wg, None, None, L.s13, L.s2, None, None, L.sh_s13,
+                                 L.sh_s2)
+
     # views of the routing results
     def ids_view(self, n):
         return self.ids[:n * self.cfg.top_k].view(n, self.cfg.top_k)
@@ -474,3 +482,58 @@ def ecospec_select(parent, q, pred_ids, n_experts: int, gamma: int, eps: float, 
     moe_ecospec_select(parent, q, pred, T, K, L, n_experts, kp, gamma, eps, b0, sel, buf, usz,
                        error_word)
     return sel[:, :n_sel], buf, usz[:T]
+
+
+class VerifyStack:
+    """L MoE layers verified in one pass ("The Limits of Speculation",
+    Sec. 3.3: the pass's cost follows the distinct experts counted in each
+    MoE layer).  Each layer routes its own hidden states, plans its union and
+    runs the deduplicating engine; the whole stack is captured in one CUDA
+    graph.  What sits between two MoE layers (attention, norms, the residual
+    stream) is not on this path, so each layer's input is given: hs is
+    [L][n_max][d], one row block per layer."""
+
+    def __init__(self, vls):
+        self.layers = list(vls)
+        self.cfg = self.layers[0].cfg
+        self.n_max = self.layers[0].n_max
+
+    @classmethod
+    def synthetic(cls, cfg: synth.LayerConfig, n_layers: int, n_max: int, seed: int = 1):
+        """n_layers seeded layers of one shape (weights seed + 10 l), each
+        generated on the device, packed, then freed of its row-major copy, so
+        that at most one row-major layer is held at a time."""
+        vls = []
+        for l in range(n_layers):
+            layer = synth.make_layer(cfg, seed=seed + 10 * l, device="cuda")
+            vl = VerifyLayer(layer, n_max)
+            vl.release_unpacked()
+            del layer
+            vls.append(vl)
+            torch.cuda.empty_cache()
+        return cls(vls)
+
+    def verify_pass(self, hs: torch.Tensor, n: int, budget: Optional[int] = None):
+        """Every layer's pass on its own rows of hs; returns the outputs."""
+        return [vl.verify_pass(hs[l, :n], n, budget=budget) for l, vl in enumerate(self.layers)]
+
+    def capture(self, hs: torch.Tensor, n: int, budget: Optional[int] = None):
+        """The whole stack's pass on hs (a fixed device buffer) as one CUDA
+        graph; replays read whatever hs holds and write each layer's y."""
+        self.verify_pass(hs, n, budget)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for l, vl in enumerate(self.layers):
+                h = hs[l, :n]
+                vl.route_plan(h, n, budget)
+                vl.dedup(h, n, kept=budget is not None)
+        return g
+
+    def unions(self):
+        """U of each layer's last plan (synchronises)."""
+        return [int(vl.plan.n_uniq[0]) for vl in self.layers]
+
+    def last_error(self) -> int:
+        errs = [vl.last_error() for vl in self.layers]
+        return next((e for e in errs if e), MOE_OK)

@@ -300,7 +300,12 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
 
   if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
+    // A segment with more tokens than one pass takes (the shared expert, a
+    // popular routed expert) streams its item's weights once per group of
+    // TOK tokens: every pass but the last loads them at normal L2 priority,
+    // so that the evict-first stream leaves them for the next pass.
     const uint64_t policy = policy_evict_first();
+    const uint64_t keep = policy_evict_normal();
     uint32_t it = 0;
     bool ok = true;
     Cursor cur;
@@ -323,7 +328,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
         mbar_arrive_expect_tx(&full[s], uint32_t(ROWS * nb));
         bulk_g2s(ring + s * STAGE_BYTES,
                  base + int64_t(cur.rb) * ROWS * kbytes + int64_t(k0) * ROWS,
-                 uint32_t(ROWS * nb), &full[s], policy);
+                 uint32_t(ROWS * nb), &full[s],
+                 cur.sg.expert >= 0 && cur.grp + 1 < cur.groups ? keep : policy);
       }
       __syncwarp();
       ++it;

@@ -115,6 +115,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// For data read again soon (the next pass over the same weights): normal
+// L2 priority, so the evict-first stream goes before it.
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // One-dimensional TMA bulk copy global -> shared, completing `bytes` of
 // transaction count on `bar`.  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -668,3 +668,18 @@ def test_ecospec_selection_is_prefix_closed_and_buffer_is_the_union():
             for l in range(L):
                 want[l, pred[v, l]] = True
         assert np.array_equal(buf, want) and cnt == want.sum()
+
+
+def test_layer_mean_union_closed_forms():
+    # "The Limits of Speculation", eq. (5), over per-layer oracle unions
+    from moe_expert_ffn_gemv_gb300 import draft_length as D
+    from moe_expert_ffn_gemv_gb300 import synth
+    row = np.array([3, 9, 27, 81, 100, 5, 6, 7], dtype=np.int32)
+    assert D.layer_mean_union([O.union_plan(np.tile(row, (n, 1)), 128)[0]
+                               for n in (1, 4, 16)]) == 8
+    n, k, E, Lyr = 6, 8, 128, 400
+    us = [O.union_plan(synth.uniform_ids(n, k, E, seed=9000 + l).numpy(), E)[0]
+          for l in range(Lyr)]
+    expect = E * (1 - (1 - k / E) ** n)
+    se = np.std(us, ddof=1) / math.sqrt(Lyr)
+    assert abs(D.layer_mean_union(us) - expect) < 3.5 * se
