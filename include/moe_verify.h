@@ -266,6 +266,29 @@ moe_status moe_verify_dedup(const moe_layer_desc *desc,
                             const moe_plan *plan, void *workspace,
                             size_t ws_bytes, void *y, moe_stream_t stream);
 
+/* One whole verification pass of the layer: moe_route_plan (or
+ * moe_route_plan_budgeted when budget >= 0), then moe_verify_dedup on its
+ * plan (with w, or w_kept under a budget), enqueued together.  Outputs are
+ * those of the separate calls, bit for bit.  Because the library knows that
+ * the kernel ahead of the expert kernels is this pass's own plan kernel,
+ * which writes nothing they read except the plan, the first expert kernel
+ * starts on the shared expert (which needs no plan) while the routing is
+ * still running; moe_verify_dedup alone cannot assume this and waits for
+ * every earlier kernel in the stream.
+ *   budget     -1 for no expert budget, else as moe_union_plan_budgeted
+ *   ids, w, logits, plan          as moe_route_plan (outputs)
+ *   w_kept, routed_union          as moe_union_plan_budgeted (budget >= 0;
+ *                                 otherwise not used and may be NULL)
+ *   workspace  as moe_verify_dedup (its header also serves the routing)
+ * n may be 0: the plan becomes empty and nothing else is enqueued. */
+moe_status moe_verify_pass(const moe_layer_desc *desc,
+                           const moe_expert_weights *weights,
+                           const void *router_w, const void *h, int32_t n,
+                           int32_t budget, int32_t *ids, float *w,
+                           float *logits, const moe_plan *plan, float *w_kept,
+                           int32_t *routed_union, void *workspace,
+                           size_t ws_bytes, void *y, moe_stream_t stream);
+
 /* The same output with the per-slot engine: each (token, slot) pair, and
  * each token's shared-expert slot, runs its expert's FFN for that one token,
  * reading the expert's weights once per pair.  No plan is needed. */

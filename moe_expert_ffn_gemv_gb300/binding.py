@@ -36,7 +36,7 @@ EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_to
             "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
             "moe_pack_expert_weights", "moe_verify_dedup_noalloc", "moe_route_plan",
             "moe_union_plan_budgeted", "moe_route_plan_budgeted", "moe_evict_select",
-            "moe_ecospec_select"]
+            "moe_ecospec_select", "moe_verify_pass"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -84,6 +84,10 @@ _lib.moe_ecospec_select.restype = ctypes.c_int
 _lib.moe_ecospec_select.argtypes = [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_double, _P, _P, _P, _P, _P, _P]
+_lib.moe_verify_pass.restype = ctypes.c_int
+_lib.moe_verify_pass.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, _P, ctypes.c_int32,
+                                 ctypes.c_int32, _P, _P, _P, ctypes.POINTER(moe_plan), _P, _P, _P,
+                                 ctypes.c_size_t, _P, _P]
 _lib.moe_verify_dedup.restype = ctypes.c_int
 _lib.moe_verify_dedup.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32, _P,
                                   _P, ctypes.POINTER(moe_plan), _P, ctypes.c_size_t, _P, _P]
@@ -199,6 +203,15 @@ def moe_ecospec_select(parent, q, pred_ids, n_trees, n_nodes, n_layers, n_expert
                                    _ptr(buffer0), _ptr(selected), _ptr(buffer_out),
                                    _ptr(union_size), _ptr(error_word), _stream(stream)),
            "moe_ecospec_select")
+
+
+def moe_verify_pass(desc, weights: moe_expert_weights, router_w, h, n, budget, ids, w, logits,
+                    plan: moe_plan, w_kept, routed_union, workspace, y, stream=None) -> None:
+    _check(_lib.moe_verify_pass(ctypes.byref(desc), ctypes.byref(weights), _ptr(router_w), _ptr(h),
+                                n, budget, _ptr(ids), _ptr(w), _ptr(logits), ctypes.byref(plan),
+                                _ptr(w_kept), _ptr(routed_union), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(y),
+                                _stream(stream)), "moe_verify_pass")
 
 
 def moe_verify_dedup(desc, weights: moe_expert_weights, h, n, ids, w, plan: moe_plan, workspace,
@@ -385,11 +398,15 @@ class VerifyLayer:
     def verify_pass(self, h: torch.Tensor, n: int, engine: str = "dedup",
                     y: Optional[torch.Tensor] = None,
                     budget: Optional[int] = None) -> torch.Tensor:
-        """Route, plan and run the experts: one MoE verification pass (with
-        the deduplicating engine, optionally under an expert budget)."""
+        """Route, plan and run the experts: one MoE verification pass (the
+        deduplicating engine through moe_verify_pass, optionally under an
+        expert budget; the per-slot engine through route + per-slot)."""
         if engine == "dedup":
-            self.route_plan(h, n, budget)
-            return self.dedup(h, n, y, kept=budget is not None)
+            y = self.y if y is None else y
+            moe_verify_pass(self.desc, self.weights, self.layer.wg, h, n,
+                            -1 if budget is None else budget, self.ids, self.w, self.logits,
+                            self._cplan, self.w_kept, self.routed_u, self.workspace, y)
+            return y[:n]
         assert budget is None, "the expert budget applies to the deduplicating engine"
         self.route(h, n)
         return self.perslot(h, n, y)
@@ -417,6 +434,17 @@ class VerifyLayer:
             else:
                 self.perslot(h, n)
         return g_route, g_experts
+
+    def capture_pass(self, h: torch.Tensor, n: int, budget: Optional[int] = None):
+        """The whole deduplicating pass (fused route + plan, then the expert
+        call) on `h` (a fixed device buffer) as one CUDA graph, so that the
+        expert kernels launch as programmatic dependents of the routing."""
+        self.verify_pass(h, n, budget=budget)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.verify_pass(h, n, budget=budget)
+        return g
 
     def last_error(self) -> int:
         return moe_last_error(self.workspace)
@@ -525,9 +553,7 @@ class VerifyStack:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for l, vl in enumerate(self.layers):
-                h = hs[l, :n]
-                vl.route_plan(h, n, budget)
-                vl.dedup(h, n, kept=budget is not None)
+                vl.verify_pass(hs[l, :n], n, budget=budget)
         return g
 
     def unions(self):

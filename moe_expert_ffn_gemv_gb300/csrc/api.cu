@@ -98,9 +98,12 @@ moe_status check_weights(const moe_layer_desc &L, const moe_expert_weights *W) {
 }
 
 // The expert FFN of one pass (both phases) and the combine, for either engine.
+// early_shared: the caller has just enqueued this pass's plan kernel on
+// `stream` (moe_verify_pass), so phase 1 may start the shared expert before
+// that kernel ends.
 moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, const void *h, int n,
                        const int32_t *ids, const float *w, const moe_plan *plan, void *workspace,
-                       void *y, cudaStream_t stream) {
+                       void *y, cudaStream_t stream, bool early_shared = false) {
   const Workspace ws = workspace_layout(L);
   uint8_t *wsb = static_cast<uint8_t *>(workspace);
   int32_t *err = reinterpret_cast<int32_t *>(wsb);
@@ -149,6 +152,7 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.T = T;
     P.err = err;
     P.timeout_ns = timeout_ns(L);
+    P.early_shared = early_shared && plan != nullptr;
     P.inter = L.inter;
     const size_t es = w_size(L);
     // phase 1: gate/up over W13, K = d
@@ -426,6 +430,24 @@ MOE_API moe_status moe_verify_dedup(const moe_layer_desc *desc, const moe_expert
   if (n == 0) return MOE_OK;
   return run_experts(*desc, *weights, h, n, ids, w, plan, workspace, y,
                      static_cast<cudaStream_t>(stream));
+}
+
+MOE_API moe_status moe_verify_pass(const moe_layer_desc *desc, const moe_expert_weights *weights,
+                                   const void *router_w, const void *h, int32_t n,
+                                   int32_t budget, int32_t *ids, float *w, float *logits,
+                                   const moe_plan *plan, float *w_kept, int32_t *routed_union,
+                                   void *workspace, size_t ws_bytes, void *y,
+                                   moe_stream_t stream) {
+  moe_status s = check_verify_args(desc, weights, h, n, n > 0 ? ids : nullptr,
+                                   n > 0 ? w : nullptr, workspace, ws_bytes, y);
+  if (s != MOE_OK) return s;
+  if (budget < -1) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  s = route_plan(desc, router_w, h, n, budget, ids, w, logits, plan, w_kept, routed_union,
+                 workspace, ws_bytes, st);
+  if (s != MOE_OK || n == 0) return s;
+  return run_experts(*desc, *weights, h, n, ids, budget >= 0 ? w_kept : w, plan, workspace, y,
+                     st, true);
 }
 
 MOE_API moe_status moe_verify_perslot(const moe_layer_desc *desc,

@@ -86,26 +86,33 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 constexpr int MAX_SLOTS = 64 * 32;
 constexpr int MAX_EXPERTS = 256;
 
+// Deduplicating segments: the shared expert first (segment 0, all n tokens;
+// it needs no plan), then the U routed experts in plan order.  Per-slot
+// segments: the n*k routed slots, then the n shared-expert slots.
 struct LocalTables {
   const int32_t *uniq;  // [U]      dedup
   const int32_t *offs;  // [U + 1]  dedup
   const int32_t *tab;   // [n*k]    dedup: perm; per-slot: ids
-  int U, n, k, n_experts, n_shared, dedup;
+  const int *U;         // U, in shared memory (read once the plan is there)
+  int n, k, n_experts, n_shared, dedup;
 
-  __device__ int n_segments() const { return dedup ? U + n_shared : n * k + n_shared * n; }
+  __device__ int n_segments() const { return dedup ? *U + n_shared : n * k + n_shared * n; }
+  // segments whose work items are known before the plan is read
+  __device__ int plan_free_segments() const { return dedup ? n_shared : 0; }
 
   __device__ Seg segment(int u) const {
     Seg s;
     const int nk = n * k;
     if (dedup) {
-      if (u < U) {
-        s.expert = uniq[u];
-        s.first = offs[u];
-        s.m = offs[u + 1] - s.first;
-      } else {
+      if (u < n_shared) {
         s.expert = -1;
         s.first = 0;
         s.m = n;
+      } else {
+        const int r = u - n_shared;
+        s.expert = uniq[r];
+        s.first = offs[r];
+        s.m = offs[r + 1] - s.first;
       }
     } else {
       s.m = 1;
@@ -135,11 +142,17 @@ struct Cursor {
   Seg sg;
 };
 
-template <int TOK>
-__device__ __forceinline__ bool cursor_item(Cursor &c, const LocalTables &T, int n_items,
-                                            int row_blocks, int32_t *err, bool report) {
-  while (c.item < n_items) {
+// ensure() makes the plan's tables usable (it may wait for them) and
+// returns false when the kernel must stop.
+template <int TOK, typename Ensure>
+__device__ __forceinline__ bool cursor_item(Cursor &c, const LocalTables &T, int row_blocks,
+                                            Ensure &ensure, int32_t *err, bool report) {
+  for (;;) {
     const int u = c.item / row_blocks;
+    if (u >= T.plan_free_segments()) {
+      if (!ensure()) return false;
+      if (u >= T.n_segments()) return false;
+    }
     c.rb = c.item - u * row_blocks;
     c.sg = T.segment(u);
     if (c.sg.expert != -2) {
@@ -151,18 +164,17 @@ __device__ __forceinline__ bool cursor_item(Cursor &c, const LocalTables &T, int
     if (report && c.rb == 0) record_error(err, MOE_ERR_DEVICE_INPUT);
     c.item += gridDim.x;
   }
-  return false;
 }
 
-template <int TOK>
-__device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int n_items,
-                                            int row_blocks, int kstages, int32_t *err,
+template <int TOK, typename Ensure>
+__device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int row_blocks,
+                                            int kstages, Ensure &ensure, int32_t *err,
                                             bool report) {
   if (++c.ks < kstages) return true;
   c.ks = 0;
   if (++c.grp < c.groups) return true;
   c.item += gridDim.x;
-  return cursor_item<TOK>(c, T, n_items, row_blocks, err, report);
+  return cursor_item<TOK>(c, T, row_blocks, ensure, err, report);
 }
 
 template <bool FP8, int PHASE, int NT>
@@ -187,18 +199,40 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   __shared__ int32_t s_offs[MAX_EXPERTS + 1];
   __shared__ int32_t s_tab[MAX_SLOTS];
   __shared__ int32_t s_U;
+  __shared__ uint64_t tables_bar;  // the plan is in shared memory (lazy phase 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = P.T.n * P.T.k;
   // Launch order: the plan, phase 1, phase 2, the combine, each of the last
-  // three launched as a programmatic dependent of the one before.  Phase 1
-  // reads the plan at once, so it waits first; it triggers only after that
-  // wait, so phase 2 never starts before the plan is complete.  Phase 2
-  // reads phase 1's activations only in its consumer warps, which wait
-  // there; its producer streams weights from the start, behind the end of
-  // phase 1.
-  if (PHASE == 1) pdl_wait();
-  pdl_trigger();
+  // three launched as a programmatic dependent of the one before.
+  //  - Phase 1 of the deduplicating engine with a shared expert, launched
+  //    right behind its pass's plan kernel (early_shared; "lazy"): the
+  //    shared expert's items need no plan, so the CTAs start on them at
+  //    once; the producer warp waits for the plan kernel only when its walk
+  //    leaves the shared segment, copies the plan to shared memory and
+  //    signals tables_bar, on which the other warps wait (bounded).  Every
+  //    CTA's producer does this (it needs U to end its walk), so phase 1
+  //    ends after the plan kernel, and it triggers phase 2 only after that
+  //    wait.
+  //  - Otherwise phase 1 waits for the plan at once; phase 2 reads the plan
+  //    (complete before phase 1 triggered it) at once and phase 1's
+  //    activations only in its consumer warps, which wait there; its
+  //    producer streams weights from the start, behind the end of phase 1.
+  const bool lazy = PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared;
+  auto load_tables = [&](int first, int step) {
+    const int32_t *src = P.T.dedup ? P.T.perm : P.T.ids;
+    for (int i = first; i < nk; i += step) s_tab[i] = src[i];
+    if (P.T.dedup)
+      for (int i = first; i <= P.T.n_experts; i += step) {
+        if (i < P.T.n_experts) s_uniq[i] = P.T.uniq[i];
+        s_offs[i] = P.T.offs[i];
+      }
+    if (first == 0) s_U = P.T.dedup ? *P.T.n_uniq : 0;
+  };
+  if (!lazy) {
+    if (PHASE == 1) pdl_wait();
+    pdl_trigger();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -208,23 +242,28 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       mbar_init(&rfull[b], CONSUMERS);
       mbar_init(&rempty[b], 1);
     }
+    mbar_init(&tables_bar, 1);
     s_abort = 0;
-    s_U = P.T.dedup ? *P.T.n_uniq : 0;
     fence_barrier_init();
   }
-  {
-    const int32_t *src = P.T.dedup ? P.T.perm : P.T.ids;
-    for (int i = threadIdx.x; i < nk; i += THREADS) s_tab[i] = src[i];
-    if (P.T.dedup)
-      for (int i = threadIdx.x; i <= P.T.n_experts; i += THREADS) {
-        if (i < P.T.n_experts) s_uniq[i] = P.T.uniq[i];
-        s_offs[i] = P.T.offs[i];
-      }
-  }
+  if (!lazy) load_tables(threadIdx.x, THREADS);
   __syncthreads();
-  LocalTables T{s_uniq, s_offs, s_tab, s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared, P.T.dedup};
+  LocalTables T{s_uniq, s_offs, s_tab, &s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared,
+                P.T.dedup};
+  // The plan gate of the warps other than the producer: a bounded wait on
+  // tables_bar the first time a walk needs the plan.
+  bool have_tables = !lazy;
+  auto await_tables = [&]() -> bool {
+    if (have_tables) return true;
+    if (!mbar_wait_bounded(&tables_bar, 0, P.timeout_ns)) {
+      s_abort = 1;
+      if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+      return false;
+    }
+    have_tables = true;
+    return true;
+  };
 
-  const int n_items = T.n_segments() * P.row_blocks;
   const int kbytes = P.kdim * ES;
   const int kstages = (kbytes + KBYTES - 1) / KBYTES;
   const int scale_cols = P.kdim / 128;              // E4M3 scale table width
@@ -239,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     uint32_t ep = 0;
     Cursor cur;
     cur.item = blockIdx.x;
-    bool have = cursor_item<TOK>(cur, T, n_items, P.row_blocks, P.err, false);
+    bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
     while (have) {
       const int b = ep % RB;
       const uint32_t round = ep / RB;
@@ -293,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       if (lane == 0) mbar_arrive(&rempty[b]);
       ++ep;
       cur.ks = kstages - 1;  // step to the next (item, token group)
-      have = cursor_next<TOK>(cur, T, n_items, P.row_blocks, kstages, P.err, false);
+      have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, await_tables, P.err, false);
     }
     return;
   }
@@ -308,9 +347,23 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     const uint64_t keep = policy_evict_normal();
     uint32_t it = 0;
     bool ok = true;
+    // The plan gate of the producer (lazy phase 1): wait for the plan
+    // kernel, let phase 2 launch, copy the plan to shared memory and signal
+    // the other warps.
+    bool plan_ready = !lazy;
+    auto load_plan = [&]() -> bool {
+      if (plan_ready) return true;
+      pdl_wait();
+      pdl_trigger();
+      load_tables(lane, 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tables_bar);
+      plan_ready = true;
+      return true;
+    };
     Cursor cur;
     cur.item = blockIdx.x;
-    bool have = cursor_item<TOK>(cur, T, n_items, P.row_blocks, P.err, false);
+    bool have = cursor_item<TOK>(cur, T, P.row_blocks, load_plan, P.err, false);
     while (have) {
       const int s = it % S;
       const uint32_t round = it / S;
@@ -333,8 +386,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
       __syncwarp();
       ++it;
-      have = cursor_next<TOK>(cur, T, n_items, P.row_blocks, kstages, P.err, false);
+      have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, load_plan, P.err, false);
     }
+    // Phase 1 must not end before the plan kernel, whatever path led here.
+    if (!plan_ready) pdl_wait();
     if (!ok) {
       if (lane == 0) {
         record_error(P.err, MOE_ERR_TIMEOUT);
@@ -419,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
 
   Cursor cur;
   cur.item = blockIdx.x;
-  bool have = cursor_item<TOK>(cur, T, n_items, P.row_blocks, P.err, tid == 0);
+  bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, tid == 0);
   int arow[NT];
   uint32_t bfr[NT][BW];
   float sc_a = 1.f, sc_b = 1.f;
@@ -431,7 +486,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   while (have) {
     // prefetch the next stage's activations and scales
     Cursor nxt = cur;
-    const bool have_next = cursor_next<TOK>(nxt, T, n_items, P.row_blocks, kstages, P.err, tid == 0);
+    const bool have_next =
+        cursor_next<TOK>(nxt, T, P.row_blocks, kstages, await_tables, P.err, tid == 0);
     int arow_n[NT];
     uint32_t bfr_n[NT][BW];
     float sc_an = 1.f, sc_bn = 1.f;

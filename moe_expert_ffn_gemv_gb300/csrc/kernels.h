@@ -46,6 +46,10 @@ struct TcParams {
   void *out;              // phase 1: a [slots][I]; phase 2: yslot [slots][d] fp32
   int32_t *err;           // workspace error word
   uint64_t timeout_ns;    // limit of every wait
+  // 1 when the kernel ahead of phase 1 in the stream is the same pass's
+  // plan kernel, which writes nothing phase 1 reads except the plan: phase 1
+  // may then start the shared expert before that kernel ends
+  int32_t early_shared;
 };
 
 // Tensor-core expert FFN (BF16 weights, or E4M3 with fp32 block scales);
