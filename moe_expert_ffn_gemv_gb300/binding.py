@@ -435,15 +435,17 @@ class VerifyLayer:
                 self.perslot(h, n)
         return g_route, g_experts
 
-    def capture_pass(self, h: torch.Tensor, n: int, budget: Optional[int] = None):
+    def capture_pass(self, h: torch.Tensor, n: int, budget: Optional[int] = None,
+                     y: Optional[torch.Tensor] = None):
         """The whole deduplicating pass (fused route + plan, then the expert
-        call) on `h` (a fixed device buffer) as one CUDA graph, so that the
-        expert kernels launch as programmatic dependents of the routing."""
-        self.verify_pass(h, n, budget=budget)
+        call) on `h` (a fixed device buffer) as one CUDA graph writing `y`
+        (self.y by default), so that the expert kernels launch as
+        programmatic dependents of the routing."""
+        self.verify_pass(h, n, y=y, budget=budget)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.verify_pass(h, n, budget=budget)
+            self.verify_pass(h, n, y=y, budget=budget)
         return g
 
     def last_error(self) -> int:
