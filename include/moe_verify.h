@@ -208,8 +208,8 @@ moe_status moe_route_plan(const moe_layer_desc *desc, const void *router_w,
 /* Verification-time expert budget (MoE-Spec, as its abstract is listed on
  * "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes, Kernel
  * Bandwidth and the Best Draft Length"; "The Limits of Speculation",
- * Sec. 2.4: a cap on the experts loaded per layer, keeping those that
- * contribute most and dropping the long tail).  moe_union_plan, except
+ * Sec. 2.4: each layer loads at most a fixed number of experts, the most
+ * useful ones, and skips the rarely used rest).  moe_union_plan, except
  * that at most `budget` routed experts enter the plan:
  *   - an expert's contribution is the sum of the weights w of the slots
  *     that name it, added in double in ascending slot order;

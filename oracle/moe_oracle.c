@@ -181,7 +181,8 @@ void orc_topk(const double *z, int n_experts, int k, int32_t *ids) {
 }
 
 /* Gate weights of the selected experts (eq. (4) and the sentence after it:
- * "normalized ... by softmax or sigmoid depending on the architecture"). */
+ * the selected scores become weights through a softmax or a sigmoid, the
+ * choice being the model's). */
 void orc_gate(const double *z, int n_experts, const int32_t *ids, int k,
               int gate, double *w) {
   if (gate == ORC_GATE_SOFTMAX) {
@@ -408,9 +409,9 @@ void orc_expert_bytes(int d, int inter, int w_type, int64_t *weights,
 
 /* ---------------------------------------------------------- expert budget */
 
-/* Verification-time expert budgeting, MoE-Spec: a fixed cap on the experts
- * loaded per layer, keeping those that contribute most to verification and
- * dropping the long tail of rarely used ones (its abstract, in the list of
+/* Verification-time expert budgeting, MoE-Spec: each layer loads at most a
+ * fixed number of experts, the most useful ones for the pass, and skips the
+ * many that few slots use (its abstract, in the list of
  * related papers on "Speculative Decoding for Mixture-of-Experts Models:
  * Expert Bytes, Kernel Bandwidth and the Best Draft Length"; "The Limits of
  * Speculation", Sec. 2.4: the per-layer expert budget is capped; "Making

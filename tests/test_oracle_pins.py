@@ -362,7 +362,7 @@ def test_expert_bytes_printed_on_the_pages():
 # ------------------------------------------------------------ expert budget
 # Verification-time expert budgeting (MoE-Spec, as its abstract is listed on
 # "Speculative Decoding for MoE Models: Expert Bytes, ..."; "The Limits of
-# Speculation", Sec. 2.4): keep the `budget` experts that contribute most,
+# Speculation", Sec. 2.4): keep the `budget` most useful experts,
 # drop the rest.  Contribution = summed gate weight (a reading).
 
 def test_budget_hand_worked_example():
