@@ -280,6 +280,10 @@ moe_status moe_verify_dedup(const moe_layer_desc *desc,
  *   w_kept, routed_union          as moe_union_plan_budgeted (budget >= 0;
  *                                 otherwise not used and may be NULL)
  *   workspace  as moe_verify_dedup (its header also serves the routing)
+ * The plan kernel hands the plan to the first expert kernel through a flag
+ * in the workspace header, which the pass's last kernel clears; after a
+ * call that failed (a non-OK status, or MOE_ERR_TIMEOUT from
+ * moe_last_error), call moe_workspace_init before reusing the workspace.
  * n may be 0: the plan becomes empty and nothing else is enqueued. */
 moe_status moe_verify_pass(const moe_layer_desc *desc,
                            const moe_expert_weights *weights,

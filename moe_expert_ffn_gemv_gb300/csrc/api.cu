@@ -109,6 +109,7 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
   int32_t *err = reinterpret_cast<int32_t *>(wsb);
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
+  uint32_t *ready = reinterpret_cast<uint32_t *>(wsb + WS_READY_OFFSET);
 
   SegTables T;
   memset(&T, 0, sizeof T);
@@ -153,6 +154,7 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.err = err;
     P.timeout_ns = timeout_ns(L);
     P.early_shared = early_shared && plan != nullptr;
+    P.ready = P.early_shared ? ready : nullptr;
     P.inter = L.inter;
     const size_t es = w_size(L);
     // phase 1: gate/up over W13, K = d
@@ -182,7 +184,8 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
   }
   if (e == cudaSuccess)
     e = launch_combine(reinterpret_cast<const float *>(wsb + ws.yslot), w, n, L.top_k, L.d,
-                       L.n_shared, L.act_dtype == MOE_BF16, y, stream);
+                       L.n_shared, L.act_dtype == MOE_BF16, y, early_shared ? ready : nullptr,
+                       stream);
   return cuda_status(e);
 }
 
@@ -311,10 +314,12 @@ moe_status union_plan(const moe_layer_desc *desc, const int32_t *ids, const floa
       plan->n_uniq, plan->offs, plan->perm, plan->union_bytes, w_kept, routed_u, error_word, st));
 }
 
+// signal_ready: raise the plan-ready flag of the workspace once the plan is
+// written (moe_verify_pass only; its combine clears the flag).
 moe_status route_plan(const moe_layer_desc *desc, const void *router_w, const void *h, int32_t n,
                       int32_t budget, int32_t *ids, float *w, float *logits, const moe_plan *plan,
                       float *w_kept, int32_t *routed_u, void *workspace, size_t ws_bytes,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool signal_ready = false) {
   moe_status s = check_desc(desc);
   if (s != MOE_OK) return s;
   if (n < 0 || n > desc->n_max) return MOE_ERR_INVALID_ARG;
@@ -337,7 +342,8 @@ moe_status route_plan(const moe_layer_desc *desc, const void *router_w, const vo
       desc->act_dtype == MOE_BF16, router_w, h, n, desc->d, desc->n_experts, desc->top_k,
       desc->gate, desc->n_shared, wb + sb, logits, ids, w, plan->hist, plan->uniq, plan->n_uniq,
       plan->offs, plan->perm, plan->union_bytes, budget, w_kept, routed_u, err,
-      reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET), st));
+      reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET),
+      signal_ready ? reinterpret_cast<unsigned int *>(wsb + WS_READY_OFFSET) : nullptr, st));
 }
 
 }  // namespace
@@ -444,7 +450,7 @@ MOE_API moe_status moe_verify_pass(const moe_layer_desc *desc, const moe_expert_
   if (budget < -1) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   s = route_plan(desc, router_w, h, n, budget, ids, w, logits, plan, w_kept, routed_union,
-                 workspace, ws_bytes, st);
+                 workspace, ws_bytes, st, /*signal_ready=*/true);
   if (s != MOE_OK || n == 0) return s;
   return run_experts(*desc, *weights, h, n, ids, budget >= 0 ? w_kept : w, plan, workspace, y,
                      st, true);

@@ -208,26 +208,30 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   //  - Phase 1 of the deduplicating engine with a shared expert, launched
   //    right behind its pass's plan kernel (early_shared; "lazy"): the
   //    shared expert's items need no plan, so the CTAs start on them at
-  //    once; the producer warp waits for the plan kernel only when its walk
-  //    leaves the shared segment, copies the plan to shared memory and
-  //    signals tables_bar, on which the other warps wait (bounded).  Every
-  //    CTA's producer does this (it needs U to end its walk), so phase 1
-  //    ends after the plan kernel, and it triggers phase 2 only after that
-  //    wait.
+  //    once.  When its walk leaves the shared segment, the producer warp
+  //    waits (bounded) for the plan kernel's plan-ready flag, copies the
+  //    plan through L2 to shared memory and signals tables_bar, on which
+  //    the other warps wait (bounded).  Once the ring is full it also waits
+  //    for the plan kernel to end (programmatic dependent launch) and only
+  //    then triggers phase 2, so phase 2 still reads a complete plan, and
+  //    phase 1 never ends before the plan kernel.
   //  - Otherwise phase 1 waits for the plan at once; phase 2 reads the plan
   //    (complete before phase 1 triggered it) at once and phase 1's
   //    activations only in its consumer warps, which wait there; its
   //    producer streams weights from the start, behind the end of phase 1.
-  const bool lazy = PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared;
-  auto load_tables = [&](int first, int step) {
+  const bool lazy =
+      PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared && P.ready != nullptr;
+  // via_l2: read through L2 (the plan kernel may still be running)
+  auto load_tables = [&](int first, int step, bool via_l2) {
+    auto rd = [via_l2](const int32_t *p) { return via_l2 ? __ldcg(p) : *p; };
     const int32_t *src = P.T.dedup ? P.T.perm : P.T.ids;
-    for (int i = first; i < nk; i += step) s_tab[i] = src[i];
+    for (int i = first; i < nk; i += step) s_tab[i] = rd(src + i);
     if (P.T.dedup)
       for (int i = first; i <= P.T.n_experts; i += step) {
-        if (i < P.T.n_experts) s_uniq[i] = P.T.uniq[i];
-        s_offs[i] = P.T.offs[i];
+        if (i < P.T.n_experts) s_uniq[i] = rd(P.T.uniq + i);
+        s_offs[i] = rd(P.T.offs + i);
       }
-    if (first == 0) s_U = P.T.dedup ? *P.T.n_uniq : 0;
+    if (first == 0) s_U = P.T.dedup ? rd(P.T.n_uniq) : 0;
   };
   if (!lazy) {
     if (PHASE == 1) pdl_wait();
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     s_abort = 0;
     fence_barrier_init();
   }
-  if (!lazy) load_tables(threadIdx.x, THREADS);
+  if (!lazy) load_tables(threadIdx.x, THREADS, false);
   __syncthreads();
   LocalTables T{s_uniq, s_offs, s_tab, &s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared,
                 P.T.dedup};
@@ -347,15 +351,30 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     const uint64_t keep = policy_evict_normal();
     uint32_t it = 0;
     bool ok = true;
-    // The plan gate of the producer (lazy phase 1): wait for the plan
-    // kernel, let phase 2 launch, copy the plan to shared memory and signal
-    // the other warps.
+    // The plan gate of the producer (lazy phase 1): wait (bounded) for the
+    // plan-ready flag, copy the plan to shared memory and signal the other
+    // warps.  The wait for the plan kernel's end, and the trigger of phase 2,
+    // come later (`joined`).
     bool plan_ready = !lazy;
+    bool joined = !lazy;
+    int since_plan = 0;  // stages issued since the plan arrived
     auto load_plan = [&]() -> bool {
       if (plan_ready) return true;
-      pdl_wait();
-      pdl_trigger();
-      load_tables(lane, 32);
+      // every lane acquires the flag itself, so that its own plan reads
+      // below are ordered after the plan kernel's writes
+      bool seen = true;
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(P.ready) == 0u)
+        if (globaltimer_ns() - t0 > P.timeout_ns) {
+          seen = false;
+          break;
+        }
+      if (!__all_sync(0xffffffffu, seen)) {
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+        s_abort = 1;
+        return false;
+      }
+      load_tables(lane, 32, true);
       __syncwarp();
       if (lane == 0) mbar_arrive(&tables_bar);
       plan_ready = true;
@@ -386,10 +405,16 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
       __syncwarp();
       ++it;
+      if (plan_ready && !joined && ++since_plan >= S) {
+        // the ring is full: wait for the plan kernel's end, then let phase 2 launch
+        pdl_wait();
+        pdl_trigger();
+        joined = true;
+      }
       have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, load_plan, P.err, false);
     }
     // Phase 1 must not end before the plan kernel, whatever path led here.
-    if (!plan_ready) pdl_wait();
+    if (!joined) pdl_wait();
     if (!ok) {
       if (lane == 0) {
         record_error(P.err, MOE_ERR_TIMEOUT);

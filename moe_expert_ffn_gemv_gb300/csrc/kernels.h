@@ -50,6 +50,7 @@ struct TcParams {
   // plan kernel, which writes nothing phase 1 reads except the plan: phase 1
   // may then start the shared expert before that kernel ends
   int32_t early_shared;
+  uint32_t *ready;  // early_shared: the plan kernel's plan-ready flag
 };
 
 // Tensor-core expert FFN (BF16 weights, or E4M3 with fp32 block scales);
@@ -87,12 +88,13 @@ cudaError_t launch_topk_gate(const float *logits, int n, int n_experts, int k, i
 // Router scores + top-k + gate + union plan in one launch; `counter` is a
 // zeroed device word that the kernel leaves zeroed.  budget >= 0: the
 // budgeted plan (w_kept written, routed_u if not NULL); budget < 0: none.
+// `ready` (or null): set to 1 with release semantics once the plan is written.
 cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, int n, int d,
                               int n_experts, int k, int gate, int n_shared, int64_t expert_bytes,
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
                               int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-                              unsigned int *counter, cudaStream_t stream);
+                              unsigned int *counter, unsigned int *ready, cudaStream_t stream);
 
 // Expert union and slot permutation (one CTA).
 cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, int n_shared,
@@ -124,7 +126,8 @@ cudaError_t launch_ecospec_select(const int32_t *parent, const float *q, const i
                                   int32_t *err, cudaStream_t stream);
 
 // y[t] = sum_j w[t][j] yslot[t*k+j] (+ yslot[n*k+t]) -> y (fp32 or bf16).
+// `ready` (or null): the plan-ready flag of moe_verify_pass, cleared here.
 cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,
-                           bool out_bf16, void *y, cudaStream_t stream);
+                           bool out_bf16, void *y, uint32_t *ready, cudaStream_t stream);
 
 }  // namespace moe

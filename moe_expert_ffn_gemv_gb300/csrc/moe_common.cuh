@@ -46,6 +46,16 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -186,6 +196,9 @@ struct Workspace {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr size_t WS_TICKET_OFFSET = 64;
+// The plan-ready flag of moe_verify_pass: raised by its plan kernel once the
+// plan is written, read by its first expert kernel, cleared by its combine.
+constexpr size_t WS_READY_OFFSET = 72;
 
 inline Workspace workspace_layout(const moe_layer_desc &L) {
   const size_t slots = size_t(L.n_max) * size_t(L.top_k + L.n_shared);

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
     int gate, int n_shared, int64_t expert_bytes, float *logits, int32_t *ids, float *w,
     int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
     int64_t *union_bytes, int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-    unsigned int *counter) {
+    unsigned int *counter, unsigned int *ready) {
   pdl_trigger();  // the expert kernel behind this one may launch (it waits for the plan)
   router_scores_cta(wg, h, n, d, n_experts, logits);
   __shared__ int s_last;
@@ -160,7 +160,14 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
                             0, hist, uniq, n_uniq, offs, perm, union_bytes, nullptr, nullptr,
                             err);
   }
-  if (threadIdx.x == 0) *counter = 0u;
+  __syncthreads();  // the whole plan is written
+  if (threadIdx.x == 0) {
+    *counter = 0u;
+    if (ready) {
+      __threadfence();
+      st_release_gpu(ready, 1u);
+    }
+  }
 }
 
 // Warps per router CTA: one per 256 columns of d, at least 8 (the fused
@@ -194,7 +201,7 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
                               int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-                              unsigned int *counter, cudaStream_t stream) {
+                              unsigned int *counter, unsigned int *ready, cudaStream_t stream) {
   dim3 grid(n_experts, (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
   const int threads = router_warps(d) * 32;
   const __nv_bfloat16 *wb = static_cast<const __nv_bfloat16 *>(router_w);
@@ -203,7 +210,7 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
   const float *hf = static_cast<const float *>(h);
 #define MOE_ROUTE_PLAN_ARGS                                                                  \
   n, d, n_experts, k, gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, \
-      perm, union_bytes, budget, w_kept, routed_u, err, counter
+      perm, union_bytes, budget, w_kept, routed_u, err, counter, ready
   if (budget < 0) {
     if (bf16)
       route_plan_kernel<__nv_bfloat16, false><<<grid, threads, 0, stream>>>(wb, hb,

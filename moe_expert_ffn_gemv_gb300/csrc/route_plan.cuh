@@ -12,63 +12,61 @@ namespace moe {
 constexpr int TOPK_MAX_PER_LANE = 8;  // N <= 256 scores per token, 8 per lane
 constexpr int PLAN_MAX_SLOTS = 64 * 32;
 
-// (v, id) beats (bv, bid): larger score, or equal score and lower id.
-__device__ __forceinline__ bool topk_beats(float v, int id, float bv, int bid) {
-  return v > bv || (v == bv && id < bid);
+// An unsigned integer with the order of the float v: the sign bit flipped
+// for v >= 0, all bits flipped for v < 0, -0 taken as +0 (so that equal
+// scores give equal keys) and NaN mapped to 0 (it never wins).
+__device__ __forceinline__ uint32_t score_key(float v) {
+  if (v != v) return 0u;
+  if (v == 0.f) v = 0.f;
+  const uint32_t b = __float_as_uint(v);
+  return (b >> 31) ? ~b : (b | 0x80000000u);
+}
+
+// The float of a key from score_key (exact; -0 comes back as +0).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // One warp: top-k of token t's scores z[0..N) (largest first, equal scores
 // by lower id: "Making Every Verified Token Count", Sec. 2.2, eq. (4)) and
-// the gate weights of the selected experts.  k rounds of a warp arg-max
-// with xor shuffles; lane j keeps the j-th selected score for the gate.
+// the gate weights of the selected experts.  Each lane holds the scores of
+// experts lane + 32 i as order keys; each of the k rounds takes the lane's
+// best remaining (key, id), then the warp's largest key and, among lanes
+// holding it, the smallest id, with one warp-reduction instruction each.
+// Lane j keeps the j-th selected score for the gate.
 __device__ __forceinline__ void topk_gate_warp(const float *z, int n_experts, int k, int gate,
                                                int32_t *ids_t, float *w_t) {
   const int lane = threadIdx.x & 31;
   float v[TOPK_MAX_PER_LANE];
-  bool taken[TOPK_MAX_PER_LANE];
+  uint32_t key[TOPK_MAX_PER_LANE];
 #pragma unroll
   for (int i = 0; i < TOPK_MAX_PER_LANE; ++i) {
     const int e = lane + 32 * i;
     v[i] = e < n_experts ? __ldcg(z + e) : -INFINITY;  // L2: other CTAs may have written z
-    taken[i] = e >= n_experts;
+    key[i] = e < n_experts ? score_key(v[i]) : 0u;     // 0: not a candidate
   }
+  uint32_t taken = 0;        // bit i: expert lane + 32 i already selected
   float my_sel = -INFINITY;  // lane j < k: score of the j-th selected expert
+  float zmax = -INFINITY;    // the largest score (the first selected)
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
+    uint32_t lk = 0u, li = 0xffffffffu;
 #pragma unroll
     for (int i = 0; i < TOPK_MAX_PER_LANE; ++i)
-      if (!taken[i] && topk_beats(v[i], lane + 32 * i, bv, bid)) {
-        bv = v[i];
-        bid = lane + 32 * i;
+      if (!((taken >> i) & 1u) && key[i] > lk) {  // ascending i: the first of equal keys
+        lk = key[i];
+        li = uint32_t(lane + 32 * i);
       }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (topk_beats(ov, oid, bv, bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) {
-#pragma unroll
-      for (int i = 0; i < TOPK_MAX_PER_LANE; ++i)
-        if (i == (bid >> 5)) taken[i] = true;
-    }
-    if (lane == j) my_sel = bv;
-    if (lane == 0) ids_t[j] = bid;
+    const uint32_t gk = __reduce_max_sync(0xffffffffu, lk);
+    const uint32_t gi = __reduce_min_sync(0xffffffffu, lk == gk ? li : 0xffffffffu);
+    if (gk != 0u && (gi & 31u) == uint32_t(lane)) taken |= 1u << (gi >> 5);
+    if (j == 0) zmax = key_score(gk);
+    if (lane == j) my_sel = key_score(gk);
+    if (lane == 0) ids_t[j] = int32_t(gi);
   }
   // gate weights
   const bool mine = lane < k;
   float num = 0.f, den = 0.f;
   if (gate == MOE_GATE_SOFTMAX) {
-    float zmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < TOPK_MAX_PER_LANE; ++i)
-      if (lane + 32 * i < n_experts) zmax = fmaxf(zmax, v[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < TOPK_MAX_PER_LANE; ++i)
