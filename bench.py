@@ -84,15 +84,20 @@ def parse():
 
 # ------------------------------------------------------------- environment
 
-def dist_setup(args):
+def dist_setup(args=None):
+    """One process per GPU (replicas only): NCCL when there is a GPU, gloo
+    when there is none (the CPU tests of the replica path)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return ws, rank
 
@@ -107,9 +112,16 @@ def max_over_ranks(x: float, ws: int) -> float:
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: float, ms_per_step: float, ws: int) -> float:
+    """The whole job's throughput: every rank moves bytes_per_rank_step per
+    step, and a step takes ms_per_step (the slowest rank's time)."""
+    return ws * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
 def measured_peaks():
@@ -267,7 +279,7 @@ def run_ours(args):
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws)
     assert vl.last_error() == 0
     ms_per_step = total_ms / args.steps
-    value = ws * union_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(union_bytes, ms_per_step, ws)
 
     # algorithmic bytes of one moe_verify_dedup call: union expert bytes + the
     # hidden states (bf16, read once), the intermediate a (fp16, written and
@@ -329,7 +341,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert vl.last_error() == 0
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / args.steps
-    e2e_value = ws * union_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_value = whole_job_gbs(union_bytes, e2e_ms, ws)
 
     sweep = None
     if not args.no_sweep and rank == 0:
