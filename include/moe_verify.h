@@ -82,7 +82,8 @@ typedef enum {
   MOE_ERR_WORKSPACE = 4,   /* workspace smaller than moe_workspace_bytes() */
   MOE_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed        */
   MOE_ERR_TIMEOUT = 6,     /* a device-side wait hit its time limit       */
-  MOE_ERR_DEVICE_INPUT = 7 /* an expert id read on the device was outside [0, N) */
+  MOE_ERR_DEVICE_INPUT = 7 /* an expert id, a tree or a plan read on the
+                              device was malformed (see each call)        */
 } moe_status;
 
 typedef enum {
@@ -259,7 +260,14 @@ moe_status moe_route_plan_budgeted(const moe_layer_desc *desc,
  *   workspace  device, ws_bytes >= moe_workspace_bytes(desc)
  *   y          device [n][d] act_dtype (out)
  * The intermediate activations are kept in fp32 (F32 weights), bf16 (BF16
- * weights) or fp16 (E4M3 weights, whose values are exact in fp16). */
+ * weights) or fp16 (E4M3 weights, whose values are exact in fp16).
+ * The kernels check the plan before they use its indices: U outside [0, N],
+ * a uniq entry outside [0, N), offs decreasing, negative or past n*k, or a
+ * perm entry outside [0, n*k) makes moe_last_error() report
+ * MOE_ERR_DEVICE_INPUT.  The bad entries are skipped, never followed (the
+ * F32 kernels skip each malformed expert group, or all of them when U is
+ * out of range; the BF16 and FP8 kernels skip every routed expert), and y
+ * is then not the layer output. */
 moe_status moe_verify_dedup(const moe_layer_desc *desc,
                             const moe_expert_weights *weights, const void *h,
                             int32_t n, const int32_t *ids, const float *w,

@@ -38,6 +38,10 @@ __global__ void __launch_bounds__(WARPS * 32) expert_f32_kernel(const F32Params 
   const int kdim = PHASE == 1 ? P.d : P.inter;
   const int row_blocks = (rows + WARPS - 1) / WARPS;
   const int n_items = n_segments(P.T) * row_blocks;
+  if (P.T.dedup && blockIdx.x == 0 && threadIdx.x == 0) {
+    const int32_t U = __ldg(P.T.n_uniq);
+    if (U < 0 || U > P.T.n_experts) record_error(P.err, MOE_ERR_DEVICE_INPUT);
+  }
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int u = item / row_blocks, rb = item - u * row_blocks;
     const Seg sg = get_segment(P.T, u);

@@ -233,6 +233,23 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
     if (first == 0) s_U = P.T.dedup ? rd(P.T.n_uniq) : 0;
   };
+  // A caller may hand moe_verify_dedup any plan: before its indices are
+  // used, check that U is at most N, every uniq entry is an expert id, offs
+  // starts at or above 0, never decreases and ends at or below n*k, and
+  // every perm entry of the groups is a slot below n*k.  Returns this
+  // thread's verdict on its share (every step-th entry from first); the
+  // caller combines the verdicts and empties a bad plan (U = 0).
+  auto plan_bad = [&](int first, int step) -> bool {
+    if (!P.T.dedup) return false;
+    const int U = s_U;
+    if (U < 0 || U > P.T.n_experts) return true;
+    if (s_offs[0] < 0 || s_offs[U] > nk) return true;
+    bool bad = false;
+    for (int r = first; r < U; r += step)
+      bad |= s_uniq[r] < 0 || s_uniq[r] >= P.T.n_experts || s_offs[r] > s_offs[r + 1];
+    for (int i = s_offs[0] + first; i < s_offs[U]; i += step) bad |= s_tab[i] < 0 || s_tab[i] >= nk;
+    return bad;
+  };
   if (!lazy) {
     if (PHASE == 1) pdl_wait();
     pdl_trigger();
@@ -252,6 +269,13 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   }
   if (!lazy) load_tables(threadIdx.x, THREADS, false);
   __syncthreads();
+  if (!lazy && __syncthreads_or(plan_bad(threadIdx.x, THREADS))) {
+    if (threadIdx.x == 0) {
+      s_U = 0;
+      record_error(P.err, MOE_ERR_DEVICE_INPUT);
+    }
+    __syncthreads();
+  }
   LocalTables T{s_uniq, s_offs, s_tab, &s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared,
                 P.T.dedup};
   // The plan gate of the warps other than the producer: a bounded wait on
@@ -375,6 +399,11 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
         return false;
       }
       load_tables(lane, 32, true);
+      __syncwarp();
+      if (__any_sync(0xffffffffu, plan_bad(lane, 32)) && lane == 0) {
+        s_U = 0;
+        record_error(P.err, MOE_ERR_DEVICE_INPUT);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&tables_bar);
       plan_ready = true;

@@ -235,8 +235,15 @@ struct Seg {
   int32_t first;   // dedup: offset into perm; per-slot: the slot index
 };
 
+// U of a deduplicating plan, or 0 when it is out of [0, N] (the plan is
+// then treated as empty; get_segment reports it).
+__device__ __forceinline__ int32_t plan_U(const SegTables &T) {
+  const int32_t U = __ldg(T.n_uniq);
+  return (U >= 0 && U <= T.n_experts) ? U : 0;
+}
+
 __device__ __forceinline__ int32_t n_segments(const SegTables &T) {
-  if (T.dedup) return __ldg(T.n_uniq) + T.n_shared;
+  if (T.dedup) return plan_U(T) + T.n_shared;
   return T.n * T.k + T.n_shared * T.n;
 }
 
@@ -244,11 +251,23 @@ __device__ __forceinline__ Seg get_segment(const SegTables &T, int32_t u) {
   Seg s;
   const int32_t nk = T.n * T.k;
   if (T.dedup) {
-    const int32_t U = __ldg(T.n_uniq);
+    const int32_t U = plan_U(T);
     if (u < U) {
+      // a caller's plan is checked before its indices are used: an expert
+      // id, a group inside [0, n*k) and slots below n*k, else skipped (-2)
       s.expert = __ldg(T.uniq + u);
       s.first = __ldg(T.offs + u);
-      s.m = __ldg(T.offs + u + 1) - s.first;
+      const int32_t last = __ldg(T.offs + u + 1);
+      s.m = last - s.first;
+      bool ok = s.expert >= 0 && s.expert < T.n_experts && s.first >= 0 && s.m >= 0 && last <= nk;
+      for (int32_t i = 0; ok && i < s.m; ++i) {
+        const int32_t p = __ldg(T.perm + s.first + i);
+        ok = p >= 0 && p < nk;
+      }
+      if (!ok) {
+        s.expert = -2;
+        s.m = 0;
+      }
     } else {
       s.expert = -1;
       s.first = 0;

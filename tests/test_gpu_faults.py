@@ -93,3 +93,42 @@ def test_pass_replays_from_a_cuda_graph(mv):
         y_eager = vl.verify_pass(h, n).clone()
         assert vl.last_error() == mv.MOE_OK
         assert torch.equal(y_graph, y_eager)
+
+
+MALFORMED = ["uniq_out_of_range", "perm_out_of_range", "u_too_large", "offs_decreasing",
+             "offs_past_slots", "offs_negative"]
+
+
+@pytest.mark.parametrize("cfg", [SMALL, synth.shrink(synth.OLMOE, 512, 128), synth.TINY],
+                         ids=lambda c: c.name)
+@pytest.mark.parametrize("kind", MALFORMED)
+def test_a_malformed_caller_plan_is_reported_not_followed(mv, cfg, kind):
+    # moe_verify_dedup takes any plan from its caller: the expert kernels
+    # check it before using its indices and report MOE_ERR_DEVICE_INPUT
+    layer = synth.make_layer(cfg, seed=4).to("cuda")
+    n = 6
+    h = synth.make_hidden(cfg, n, seed=5).cuda()
+    vl = mv.VerifyLayer(layer, n)
+    vl.route(h, n)
+    vl.union_plan(n)
+    y_ok = vl.dedup(h, n).clone()
+    assert vl.last_error() == mv.MOE_OK
+    U = int(vl.plan.n_uniq[0])
+    if kind == "uniq_out_of_range":
+        vl.plan.uniq[U // 2] = cfg.n_experts + 7
+    elif kind == "perm_out_of_range":
+        vl.plan.perm[1] = 1 << 20
+    elif kind == "u_too_large":
+        vl.plan.n_uniq[0] = cfg.n_experts + 1
+    elif kind == "offs_decreasing":
+        vl.plan.offs[1] = int(vl.plan.offs[2]) + 1
+    elif kind == "offs_past_slots":
+        vl.plan.offs[U] = n * cfg.top_k + 5
+    else:
+        vl.plan.offs[0] = -3
+    vl.dedup(h, n)
+    assert vl.last_error() == mv.MOE_ERR_DEVICE_INPUT
+    # a good plan afterwards gives the right output again
+    vl.union_plan(n)
+    assert torch.equal(vl.dedup(h, n), y_ok)
+    assert vl.last_error() == mv.MOE_OK
