@@ -53,13 +53,15 @@
  *     and s the fp32 scale of its 128 x 128 block.
  *   - Packed weights: moe_verify_dedup and moe_verify_perslot read w13, w2,
  *     sh_w13 and sh_w2 in the tile layout that moe_pack_expert_weights
- *     writes once, when the model is loaded (same size as the row-major
- *     arrays; identical to them for F32).  Scales stay row-major.
+ *     writes once, when the model is loaded (moe_packed_bytes gives the
+ *     sizes: those of the row-major arrays, plus for E4M3 the block scales,
+ *     which the packed tiles carry; identical to the row-major arrays for
+ *     F32).
  *   - Limits (else MOE_ERR_UNSUPPORTED): N <= 256, 1 <= k <= min(N, 32),
  *     0 <= n <= n_max <= 64, n_shared 0 or 1, d % 8 == 0; F32 weights go with
  *     F32 activations and need I % 4 == 0; BF16 and E4M3 weights go with BF16
  *     activations; BF16 needs d % 64 == 0 and I % 32 == 0, E4M3 needs
- *     d % 128 == 0 and I % 128 == 0.
+ *     d % 128 == 0, I % 128 == 0, d <= 8192 and I <= 8192.
  */
 #ifndef MOE_VERIFY_H
 #define MOE_VERIFY_H
@@ -111,15 +113,13 @@ typedef struct {
   int32_t wait_timeout_us; /* limit of every device-side wait; 0 = 1 s    */
 } moe_layer_desc;
 
+/* The experts as moe_pack_expert_weights wrote them (E4M3: with their
+ * block scales). */
 typedef struct {
-  const void *w13;    /* device, [N][2I][d], packed                 */
-  const void *w2;     /* device, [N][d][I], packed                  */
-  const float *s13;   /* device, E4M3 only, else NULL               */
-  const float *s2;    /* device, E4M3 only, else NULL               */
-  const void *sh_w13; /* device, shared expert [2I][d]; NULL if none */
-  const void *sh_w2;  /* device, shared expert [d][I]                */
-  const float *sh_s13;
-  const float *sh_s2;
+  const void *w13;    /* device, N packed W13 matrices              */
+  const void *w2;     /* device, N packed W2 matrices               */
+  const void *sh_w13; /* device, the shared expert's packed W13; NULL if none */
+  const void *sh_w2;  /* device, the shared expert's packed W2      */
 } moe_expert_weights;
 
 /* The union plan (all device arrays, owned by the caller). */
@@ -147,18 +147,28 @@ size_t moe_workspace_bytes(const moe_layer_desc *desc);
 moe_status moe_expert_bytes(const moe_layer_desc *desc, int64_t *weight_bytes,
                             int64_t *scale_bytes);
 
+/* Bytes of one expert's packed W13 and W2 (either pointer may be NULL). */
+moe_status moe_packed_bytes(const moe_layer_desc *desc, int64_t *w13_bytes,
+                            int64_t *w2_bytes);
+
 /* Repacks n_matrices experts' W13 and W2 (device, row-major as in the layout
  * above) into the tile layout the expert engines stream (device, caller
- * allocated, same sizes, not in place).  BF16 and E4M3: each expert matrix
- * becomes a sequence of tiles of 64 rows x 512 bytes (the last tile of a row
- * block narrower when a row is not a multiple of 512 bytes); a W13 tile
- * holds gate rows 32b..32b+31 followed by up rows I+32b..I+32b+31; inside a
- * tile the 16-byte pieces are ordered [64-byte column chunk][16-row tile]
- * [row half][lane] so that one pipeline stage is one contiguous bulk copy.
- * F32: a plain copy.  Call once per layer (N routed experts) and once for
- * the shared expert (n_matrices = 1). */
+ * allocated, n_matrices times moe_packed_bytes, not in place).  BF16 and
+ * E4M3: each expert matrix becomes a sequence of tiles of 64 rows x 512
+ * bytes (the last tile of a row block narrower when a row is not a multiple
+ * of 512 bytes); a W13 tile holds gate rows 32b..32b+31 followed by up rows
+ * I+32b..I+32b+31; inside a tile the 16-byte pieces are ordered [64-byte
+ * column chunk][16-row tile][row half][lane] so that one pipeline stage is
+ * one contiguous bulk copy.  E4M3: every tile is followed by its 8 block
+ * scales from s13 / s2 (device, [n_matrices][rows/128][cols/128] float as in
+ * the layout above; NULL for other weight types): the scales of the tile's
+ * four 128-column blocks for the 128-row block of its first 32 rows, then
+ * of its last 32 rows (0 past the last column block).  F32: a plain copy.
+ * Call once per layer (N routed experts) and once for the shared expert
+ * (n_matrices = 1). */
 moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const void *w13,
-                                   const void *w2, int32_t n_matrices,
+                                   const void *w2, const float *s13,
+                                   const float *s2, int32_t n_matrices,
                                    void *w13_packed, void *w2_packed,
                                    moe_stream_t stream);
 

@@ -11,7 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 from dataclasses import dataclass
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -36,7 +36,7 @@ EXPORTED = ["moe_workspace_bytes", "moe_expert_bytes", "moe_route_topk", "moe_to
             "moe_last_error", "moe_selftest_bounded_wait", "moe_status_string",
             "moe_pack_expert_weights", "moe_verify_dedup_noalloc", "moe_route_plan",
             "moe_union_plan_budgeted", "moe_route_plan_budgeted", "moe_evict_select",
-            "moe_ecospec_select", "moe_verify_pass"]
+            "moe_ecospec_select", "moe_verify_pass", "moe_packed_bytes"]
 
 
 class moe_layer_desc(ctypes.Structure):
@@ -47,7 +47,7 @@ class moe_layer_desc(ctypes.Structure):
 
 class moe_expert_weights(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in
-                ("w13", "w2", "s13", "s2", "sh_w13", "sh_w2", "sh_s13", "sh_s2")]
+                ("w13", "w2", "sh_w13", "sh_w2")]
 
 
 class moe_plan(ctypes.Structure):
@@ -98,7 +98,9 @@ _lib.moe_verify_dedup_noalloc.restype = ctypes.c_int
 _lib.moe_verify_dedup_noalloc.argtypes = [_D, ctypes.POINTER(moe_expert_weights), _P, ctypes.c_int32,
                                           _P, _P, ctypes.POINTER(moe_plan), _P, _P, _P]
 _lib.moe_pack_expert_weights.restype = ctypes.c_int
-_lib.moe_pack_expert_weights.argtypes = [_D, _P, _P, ctypes.c_int32, _P, _P, _P]
+_lib.moe_pack_expert_weights.argtypes = [_D, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P]
+_lib.moe_packed_bytes.restype = ctypes.c_int
+_lib.moe_packed_bytes.argtypes = [_D, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
 _lib.moe_workspace_init.restype = ctypes.c_int
 _lib.moe_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
 _lib.moe_last_error.restype = ctypes.c_int
@@ -240,9 +242,19 @@ def moe_verify_perslot(desc, weights: moe_expert_weights, h, n, ids, w, workspac
                                    _stream(stream)), "moe_verify_perslot")
 
 
-def moe_pack_expert_weights(desc, w13, w2, n_matrices, w13_packed, w2_packed, stream=None) -> None:
-    _check(_lib.moe_pack_expert_weights(ctypes.byref(desc), _ptr(w13), _ptr(w2), n_matrices,
-                                        _ptr(w13_packed), _ptr(w2_packed), _stream(stream)),
+def moe_packed_bytes(desc) -> Tuple[int, int]:
+    """(W13, W2) bytes of one packed expert."""
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(_lib.moe_packed_bytes(ctypes.byref(desc), ctypes.byref(a), ctypes.byref(b)),
+           "moe_packed_bytes")
+    return a.value, b.value
+
+
+def moe_pack_expert_weights(desc, w13, w2, s13, s2, n_matrices, w13_packed, w2_packed,
+                            stream=None) -> None:
+    _check(_lib.moe_pack_expert_weights(ctypes.byref(desc), _ptr(w13), _ptr(w2), _ptr(s13),
+                                        _ptr(s2), n_matrices, _ptr(w13_packed), _ptr(w2_packed),
+                                        _stream(stream)),
            "moe_pack_expert_weights")
 
 
@@ -280,28 +292,28 @@ class PackedWeights:
     w2: torch.Tensor
     sh_w13: Optional[torch.Tensor]
     sh_w2: Optional[torch.Tensor]
-    s13: Optional[torch.Tensor]
-    s2: Optional[torch.Tensor]
-    sh_s13: Optional[torch.Tensor]
-    sh_s2: Optional[torch.Tensor]
 
     def c(self) -> moe_expert_weights:
-        return moe_expert_weights(_ptr(self.w13), _ptr(self.w2), _ptr(self.s13), _ptr(self.s2),
-                                  _ptr(self.sh_w13), _ptr(self.sh_w2), _ptr(self.sh_s13),
-                                  _ptr(self.sh_s2))
+        return moe_expert_weights(_ptr(self.w13), _ptr(self.w2), _ptr(self.sh_w13),
+                                  _ptr(self.sh_w2))
 
 
 def pack_weights(layer: synth.Layer, desc: moe_layer_desc) -> PackedWeights:
-    """Repack a layer's (device, row-major) expert weights with moe_pack_expert_weights."""
-    w13 = torch.empty_like(layer.w13)
-    w2 = torch.empty_like(layer.w2)
-    moe_pack_expert_weights(desc, layer.w13, layer.w2, layer.cfg.n_experts, w13, w2)
+    """Repack a layer's (device, row-major) expert weights, and for E4M3 their
+    block scales, with moe_pack_expert_weights."""
+    b13, b2 = moe_packed_bytes(desc)
+    dev = layer.w13.device
+    N = layer.cfg.n_experts
+    w13 = torch.empty(N * b13, dtype=torch.uint8, device=dev)
+    w2 = torch.empty(N * b2, dtype=torch.uint8, device=dev)
+    moe_pack_expert_weights(desc, layer.w13, layer.w2, layer.s13, layer.s2, N, w13, w2)
     sh13 = sh2 = None
     if layer.sh_w13 is not None:
-        sh13 = torch.empty_like(layer.sh_w13)
-        sh2 = torch.empty_like(layer.sh_w2)
-        moe_pack_expert_weights(desc, layer.sh_w13, layer.sh_w2, 1, sh13, sh2)
-    return PackedWeights(w13, w2, sh13, sh2, layer.s13, layer.s2, layer.sh_s13, layer.sh_s2)
+        sh13 = torch.empty(b13, dtype=torch.uint8, device=dev)
+        sh2 = torch.empty(b2, dtype=torch.uint8, device=dev)
+        moe_pack_expert_weights(desc, layer.sh_w13, layer.sh_w2, layer.sh_s13, layer.sh_s2, 1,
+                                sh13, sh2)
+    return PackedWeights(w13, w2, sh13, sh2)
 
 
 @dataclass

@@ -85,14 +85,9 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 moe_status check_weights(const moe_layer_desc &L, const moe_expert_weights *W) {
   if (!W || !W->w13 || !W->w2) return MOE_ERR_INVALID_ARG;
   if (!aligned16(W->w13) || !aligned16(W->w2)) return MOE_ERR_ALIGNMENT;
-  const bool fp8 = L.w_dtype == MOE_E4M3_B128;
-  if (fp8 && (!W->s13 || !W->s2)) return MOE_ERR_INVALID_ARG;
-  if (fp8 && (!aligned16(W->s13) || !aligned16(W->s2))) return MOE_ERR_ALIGNMENT;
   if (L.n_shared) {
     if (!W->sh_w13 || !W->sh_w2) return MOE_ERR_INVALID_ARG;
     if (!aligned16(W->sh_w13) || !aligned16(W->sh_w2)) return MOE_ERR_ALIGNMENT;
-    if (fp8 && (!W->sh_s13 || !W->sh_s2)) return MOE_ERR_INVALID_ARG;
-    if (fp8 && (!aligned16(W->sh_s13) || !aligned16(W->sh_s2))) return MOE_ERR_ALIGNMENT;
   }
   return MOE_OK;
 }
@@ -160,9 +155,7 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     // phase 1: gate/up over W13, K = d
     P.w = static_cast<const uint8_t *>(W.w13);
     P.w_sh = static_cast<const uint8_t *>(W.sh_w13);
-    P.sc = W.s13;
-    P.sc_sh = W.sh_s13;
-    P.expert_stride = int64_t(2) * L.inter * L.d * int64_t(es);
+    P.expert_stride = packed_matrix_bytes(2 * L.inter, int(L.d * es), fp8);
     P.rows_total = 2 * L.inter;
     P.kdim = L.d;
     P.row_blocks = L.inter / 32;
@@ -172,9 +165,7 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     // phase 2: down over W2, K = I
     P.w = static_cast<const uint8_t *>(W.w2);
     P.w_sh = static_cast<const uint8_t *>(W.sh_w2);
-    P.sc = W.s2;
-    P.sc_sh = W.sh_s2;
-    P.expert_stride = int64_t(L.d) * L.inter * int64_t(es);
+    P.expert_stride = packed_matrix_bytes(L.d, int(L.inter * es), fp8);
     P.rows_total = L.d;
     P.kdim = L.inter;
     P.row_blocks = L.d / 64;
@@ -539,9 +530,26 @@ MOE_API moe_status moe_verify_dedup_noalloc(const moe_layer_desc *desc,
   return MOE_OK;
 }
 
+MOE_API moe_status moe_packed_bytes(const moe_layer_desc *desc, int64_t *w13_bytes,
+                                    int64_t *w2_bytes) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  const moe_layer_desc &L = *desc;
+  const int es = int(w_size(L));
+  const bool fp8 = L.w_dtype == MOE_E4M3_B128;
+  const bool tiled = L.w_dtype != MOE_F32;
+  if (w13_bytes)
+    *w13_bytes = tiled ? packed_matrix_bytes(2 * L.inter, L.d * es, fp8)
+                       : int64_t(2) * L.inter * L.d * es;
+  if (w2_bytes)
+    *w2_bytes = tiled ? packed_matrix_bytes(L.d, L.inter * es, fp8) : int64_t(L.d) * L.inter * es;
+  return MOE_OK;
+}
+
 MOE_API moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const void *w13,
-                                           const void *w2, int32_t n_matrices, void *w13_packed,
-                                           void *w2_packed, moe_stream_t stream) {
+                                           const void *w2, const float *s13, const float *s2,
+                                           int32_t n_matrices, void *w13_packed, void *w2_packed,
+                                           moe_stream_t stream) {
   moe_status s = check_desc(desc);
   if (s != MOE_OK) return s;
   if (n_matrices < 0) return MOE_ERR_INVALID_ARG;
@@ -551,6 +559,9 @@ MOE_API moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const voi
     return MOE_ERR_ALIGNMENT;
   if (w13 == w13_packed || w2 == w2_packed) return MOE_ERR_INVALID_ARG;  // not in place
   const moe_layer_desc &L = *desc;
+  const bool fp8 = L.w_dtype == MOE_E4M3_B128;
+  if (fp8 && (!s13 || !s2)) return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!aligned16(s13) || !aligned16(s2))) return MOE_ERR_ALIGNMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t es = w_size(L);
   const size_t n13 = size_t(n_matrices) * 2 * L.inter * L.d * es;
@@ -561,9 +572,11 @@ MOE_API moe_status moe_pack_expert_weights(const moe_layer_desc *desc, const voi
     e = cudaMemcpyAsync(w13_packed, w13, n13, cudaMemcpyDeviceToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(w2_packed, w2, n2, cudaMemcpyDeviceToDevice, st);
   } else {
-    e = launch_pack(w13, w13_packed, n_matrices, 2 * L.inter, int(L.d * es), L.inter, true, st);
+    e = launch_pack(w13, fp8 ? s13 : nullptr, w13_packed, n_matrices, 2 * L.inter, int(L.d * es),
+                    L.inter, true, st);
     if (e == cudaSuccess)
-      e = launch_pack(w2, w2_packed, n_matrices, L.d, int(L.inter * es), L.inter, false, st);
+      e = launch_pack(w2, fp8 ? s2 : nullptr, w2_packed, n_matrices, L.d, int(L.inter * es),
+                      L.inter, false, st);
   }
   return cuda_status(e);
 }

@@ -17,11 +17,17 @@
 // Structure (one CTA per SM, persistent over work items (segment, row block)):
 //   - the weights are stored pre-packed (pack.cu): the 64 rows x 512 bytes of
 //     one pipeline stage form one contiguous tile, its 16-byte pieces in the
-//     order the consumer threads read them;
-//   - warp 8 is the producer: it streams one tile per stage with a single 1-D
-//     TMA bulk copy (cp.async.bulk, completing on an mbarrier) into a 4- to
-//     6-stage shared-memory ring.  Copies of a few KB keep the copy engine at
-//     HBM speed; 512-byte copies (one per row) would not;
+//     order the consumer threads read them, an E4M3 tile followed by its 8
+//     block scales;
+//   - warp 8 is the producer: per stage it fills one slot of a 5-stage
+//     shared-memory ring with a 1-D TMA bulk copy (cp.async.bulk, completing
+//     on the slot's mbarrier) of the tile and its scales, and one bulk copy
+//     per token of the K chunk of that token's activation row.  So the
+//     consumers read nothing but shared memory: a global load issued by a
+//     consumer returns behind the SM's stream of weight tiles, several
+//     stages late, and stalls it.  The producer's issue time per copy is
+//     what keeps it from running further ahead, so a stage costs it as few
+//     copies as possible (no separate scale copy);
 //   - warps 0..7 consume: warp w owns bytes [64 w, 64 w + 64) of every row of a
 //     stage, i.e. a K-split across warps, and runs mma.sync m16n8k16 with the
 //     weights as the 16-row A operand (4 row tiles) and the segment's tokens as
@@ -29,17 +35,17 @@
 //     on the order of its terms, each thread's 16 contiguous weight bytes feed
 //     the A fragment directly (no ldmatrix); the activations (B fragment) are
 //     read with the same permutation of K.  Each warp reads its 4 KB of a
-//     stage with lane-contiguous 16-byte loads (no bank conflicts);
+//     stage with lane-contiguous 16-byte loads (no bank conflicts), and its
+//     tokens' activations from rows padded apart so that they hit distinct
+//     banks;
 //   - E4M3 bytes become fp16 with cvt.rn.f16x2.e4m3x2 (exact); the block scale
 //     multiplies the fp32 partial sum of each 64-column chunk, which lies in a
 //     single 128x128 scale block;
-//   - the activation fragments and scales of the next stage are loaded while
-//     the current stage computes; the plan sits in shared memory;
 //   - after the last stage of an item each consumer warp drops its partial
-//     sums into one of two reduction buffers and goes on streaming; warp 9,
-//     the epilogue warp, adds the 8 warps' partials in a fixed order
-//     (deterministic) and applies silu(g)*u (phase 1) or stores the fp32 rows
-//     (phase 2), so no consumer waits for another at item boundaries.
+//     sums into a reduction buffer (two for BF16, one for E4M3, whose ring
+//     slots are larger) and goes on streaming; warp 9, the epilogue warp,
+//     adds the 8 warps' partials in a fixed order (deterministic) and applies
+//     silu(g)*u (phase 1) or stores the fp32 rows (phase 2).
 // Every wait is bounded; on time-out the kernel records MOE_ERR_TIMEOUT in the
 // workspace error word, keeps its barrier structure, lets its own copies land
 // and returns.
@@ -59,21 +65,39 @@ constexpr int EPILOGUE = CONSUMERS + 1;            // warp 9
 constexpr int THREADS = (CONSUMERS + 2) * 32;
 constexpr uint64_t DRAIN_LIMIT_NS = 200ull * 1000 * 1000;
 
-// Shared memory: the weight ring, then the cross-warp reduction buffers
-// (consumers hand an item's partial sums to the epilogue warp there).
-template <int NT>
-constexpr int n_red_bufs() { return NT >= 4 ? 1 : 2; }
+// Shared memory: a ring of S slots, each with one stage's weight tile (E4M3:
+// with its 8 block scales behind it) and the activation rows of its tokens;
+// the cross-warp reduction buffers (consumers hand an item's partial sums to
+// the epilogue warp there); the barriers.
+template <bool FP8, int NT>
+constexpr int n_red_bufs() { return FP8 || NT >= 4 ? 1 : 2; }
 
 template <int NT>
 constexpr size_t red_bytes() { return size_t(CONSUMERS) * 4 * NT * 32 * 16; }
 
-template <int NT>
-constexpr int n_stages() { return NT >= 4 ? 4 : NT == 2 ? 4 : 5; }
+// One activation row of a stage: its K columns as 16-bit values, plus a pad
+// that puts consecutive rows 4 (E4M3) or 16 (BF16) banks apart, so that the
+// consumers' 16-byte reads of two tokens' rows never meet in a bank.
+template <bool FP8>
+constexpr int act_row_bytes() { return KBYTES / (FP8 ? 1 : 2) * 2 + (FP8 ? 16 : 64); }
 
-template <int NT>
+// where a slot's activation rows start: behind the largest tile
+template <bool FP8>
+constexpr int act_offset() { return STAGE_BYTES + (FP8 ? PACK_SCALE_BYTES : 0); }
+
+template <bool FP8, int NT>
+constexpr int slot_bytes() {
+  return (act_offset<FP8>() + 8 * NT * act_row_bytes<FP8>() + 127) / 128 * 128;
+}
+
+template <bool FP8, int NT>
+constexpr int n_stages() { return NT >= 2 ? 4 : 5; }
+
+template <bool FP8, int NT>
 constexpr size_t smem_bytes() {
-  return size_t(n_stages<NT>()) * STAGE_BYTES + n_red_bufs<NT>() * red_bytes<NT>() +
-         2 * (n_stages<NT>() + n_red_bufs<NT>()) * 8;
+  return size_t(n_stages<FP8, NT>()) * slot_bytes<FP8, NT>() +
+         n_red_bufs<FP8, NT>() * red_bytes<NT>() +
+         2 * (n_stages<FP8, NT>() + n_red_bufs<FP8, NT>()) * 8;
 }
 
 __device__ __forceinline__ float silu_times(float g, float u) {
@@ -92,7 +116,7 @@ constexpr int MAX_EXPERTS = 256;
 struct LocalTables {
   const int32_t *uniq;  // [U]      dedup
   const int32_t *offs;  // [U + 1]  dedup
-  const int32_t *tab;   // [n*k]    dedup: perm; per-slot: ids
+  const int16_t *tab;   // [n*k]    dedup: perm; per-slot: ids (-1: out of range)
   const int *U;         // U, in shared memory (read once the plan is there)
   int n, k, n_experts, n_shared, dedup;
 
@@ -179,17 +203,21 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
 
 template <bool FP8, int PHASE, int NT>
 __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P) {
-  constexpr int S = n_stages<NT>();
-  constexpr int RB = n_red_bufs<NT>();
+  constexpr int S = n_stages<FP8, NT>();
+  constexpr int SLOT = slot_bytes<FP8, NT>();
+  constexpr int RB = n_red_bufs<FP8, NT>();
   constexpr int ES = FP8 ? 1 : 2;       // bytes per weight element
   constexpr int TOK = 8 * NT;           // tokens per pass over an item
   constexpr int BW = FP8 ? 8 : 4;       // B-fragment words per N tile and stage
+  constexpr int ACT_ROW = act_row_bytes<FP8>();
+  constexpr int ACT_OFF = act_offset<FP8>();  // a slot's activation rows
+  constexpr int TRAILER = FP8 ? PACK_SCALE_BYTES : 0;  // scale bytes behind a tile
   // E4M3 phase 1 reads the bf16 hidden states and converts them to fp16
   constexpr bool BF16_ACT_TO_F16 = FP8 && PHASE == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
-  float4 *red = reinterpret_cast<float4 *>(smem + S * STAGE_BYTES);   // [RB][red_bytes]
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * STAGE_BYTES + RB * red_bytes<NT>());
+  float4 *red = reinterpret_cast<float4 *>(smem + S * SLOT);   // [RB][red_bytes]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * SLOT + RB * red_bytes<NT>());
   uint64_t *empty = full + S;
   uint64_t *rfull = empty + S;    // consumers -> epilogue warp (count CONSUMERS)
   uint64_t *rempty = rfull + RB;  // epilogue warp -> consumers (count 1)
@@ -197,7 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   __shared__ volatile int s_abort;
   __shared__ int32_t s_uniq[MAX_EXPERTS];
   __shared__ int32_t s_offs[MAX_EXPERTS + 1];
-  __shared__ int32_t s_tab[MAX_SLOTS];
+  __shared__ int16_t s_tab[MAX_SLOTS];  // entries below 2048; -1 stands for any other
   __shared__ int32_t s_U;
   __shared__ uint64_t tables_bar;  // the plan is in shared memory (lazy phase 1)
 
@@ -216,16 +244,21 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   //    then triggers phase 2, so phase 2 still reads a complete plan, and
   //    phase 1 never ends before the plan kernel.
   //  - Otherwise phase 1 waits for the plan at once; phase 2 reads the plan
-  //    (complete before phase 1 triggered it) at once and phase 1's
-  //    activations only in its consumer warps, which wait there; its
-  //    producer streams weights from the start, behind the end of phase 1.
+  //    (complete before phase 1 triggered it) at once.  Its producer streams
+  //    the first S stages' weights from the start, behind the end of phase
+  //    1, then waits for phase 1 to end before it copies phase 1's
+  //    activations (and only then closes those stages).
   const bool lazy =
       PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared && P.ready != nullptr;
   // via_l2: read through L2 (the plan kernel may still be running)
   auto load_tables = [&](int first, int step, bool via_l2) {
     auto rd = [via_l2](const int32_t *p) { return via_l2 ? __ldcg(p) : *p; };
     const int32_t *src = P.T.dedup ? P.T.perm : P.T.ids;
-    for (int i = first; i < nk; i += step) s_tab[i] = rd(src + i);
+    const int lim = P.T.dedup ? nk : P.T.n_experts;
+    for (int i = first; i < nk; i += step) {
+      const int32_t v = rd(src + i);
+      s_tab[i] = int16_t(v >= 0 && v < lim ? v : -1);
+    }
     if (P.T.dedup)
       for (int i = first; i <= P.T.n_experts; i += step) {
         if (i < P.T.n_experts) s_uniq[i] = rd(P.T.uniq + i);
@@ -294,8 +327,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
 
   const int kbytes = P.kdim * ES;
   const int kstages = (kbytes + KBYTES - 1) / KBYTES;
-  const int scale_cols = P.kdim / 128;              // E4M3 scale table width
-  const int64_t scale_stride = int64_t(P.rows_total / 128) * scale_cols;
+  // packed bytes of one row block: its tiles, each followed by its scales
+  const int64_t rb_bytes = int64_t(ROWS) * kbytes + int64_t(kstages) * TRAILER;
 
   if (warp == EPILOGUE) {
     // -------------------------------------------------------------- epilogue
@@ -409,6 +442,56 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       plan_ready = true;
       return true;
     };
+    // Fills slot s with stage q: the packed tile of (row block, K chunk),
+    // contiguous, ROWS * nb bytes of weights followed (E4M3) by the tile's
+    // block scales (weights); the K chunk of each of the stage's tokens'
+    // activation rows, one bulk copy per row (acts).  The barrier's phase
+    // closes (the producer's arrival) with the activations: before them
+    // only the tile's bytes are announced.  The consumers read nothing but
+    // shared memory (a global load of theirs would come back behind the
+    // SM's stream of weight tiles), and the producer issues as few copies
+    // as it can: each costs it issue time, and it must keep ahead of HBM.
+    const uint8_t *act = static_cast<const uint8_t *>(P.act);
+    auto issue_stage = [&](const Cursor &q, int s, bool weights, bool acts) {
+      uint8_t *slot = ring + s * SLOT;
+      const int k0 = q.ks * KBYTES;
+      const int nb = min(KBYTES, kbytes - k0);
+      const uint32_t tile_bytes = uint32_t(ROWS * nb + TRAILER);
+      const uint32_t row_bytes = uint32_t(nb / ES) * 2;
+      const int m_rows = acts ? max(0, min(TOK, q.sg.m - q.grp * TOK)) : 0;
+      if (lane == 0) {
+        const uint32_t tx = (weights ? tile_bytes : 0u) + uint32_t(m_rows) * row_bytes;
+        if (acts) mbar_arrive_expect_tx(&full[s], tx);
+        else mbar_expect_tx(&full[s], tx);
+      }
+      __syncwarp();
+      if (weights && lane == 0) {
+        const uint8_t *base =
+            q.sg.expert >= 0 ? P.w + int64_t(q.sg.expert) * P.expert_stride : P.w_sh;
+        bulk_g2s(slot, base + q.rb * rb_bytes + int64_t(q.ks) * (ROWS * KBYTES + TRAILER),
+                 tile_bytes, &full[s], q.sg.expert >= 0 && q.grp + 1 < q.groups ? keep : policy);
+      }
+      for (int j = lane; j < m_rows; j += 32) {
+        const int sl = T.slot(q.sg, q.grp * TOK + j);
+        const int row = PHASE == 1 ? T.token(sl) : sl;
+        bulk_g2s(slot + ACT_OFF + j * ACT_ROW, act + (int64_t(row) * P.kdim + k0 / ES) * 2,
+                 row_bytes, &full[s], keep);
+      }
+    };
+    // Phase 2: the activations of the stages issued so far (at most S),
+    // once phase 1 has ended.
+    bool acts_ok = PHASE == 1;
+    auto late_acts = [&]() {
+      pdl_wait();
+      Cursor q;
+      q.item = blockIdx.x;
+      bool h = cursor_item<TOK>(q, T, P.row_blocks, load_plan, P.err, false);
+      for (uint32_t j = 0; j < it && h; ++j) {
+        issue_stage(q, int(j), false, true);
+        h = cursor_next<TOK>(q, T, P.row_blocks, kstages, load_plan, P.err, false);
+      }
+      acts_ok = true;
+    };
     Cursor cur;
     cur.item = blockIdx.x;
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, load_plan, P.err, false);
@@ -420,20 +503,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
         break;
       }
       if (s_abort) { ok = false; break; }
-      const uint8_t *base =
-          cur.sg.expert >= 0 ? P.w + int64_t(cur.sg.expert) * P.expert_stride : P.w_sh;
-      const int k0 = cur.ks * KBYTES;
-      const int nb = min(KBYTES, kbytes - k0);
-      // the packed tile of (row block, K chunk): contiguous, ROWS * nb bytes
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&full[s], uint32_t(ROWS * nb));
-        bulk_g2s(ring + s * STAGE_BYTES,
-                 base + int64_t(cur.rb) * ROWS * kbytes + int64_t(k0) * ROWS,
-                 uint32_t(ROWS * nb), &full[s],
-                 cur.sg.expert >= 0 && cur.grp + 1 < cur.groups ? keep : policy);
-      }
-      __syncwarp();
+      issue_stage(cur, s, true, acts_ok);
       ++it;
+      if (!acts_ok && it == uint32_t(S)) late_acts();
       if (plan_ready && !joined && ++since_plan >= S) {
         // the ring is full: wait for the plan kernel's end, then let phase 2 launch
         pdl_wait();
@@ -442,8 +514,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
       have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, load_plan, P.err, false);
     }
-    // Phase 1 must not end before the plan kernel, whatever path led here.
+    // Phase 1 must not end before the plan kernel, whatever path led here;
+    // phase 2 closes the stages still waiting for their activations.
     if (!joined) pdl_wait();
+    if (!acts_ok) late_acts();
     if (!ok) {
       if (lane == 0) {
         record_error(P.err, MOE_ERR_TIMEOUT);
@@ -462,61 +536,11 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   }
 
   // -------------------------------------------------------------- consumers
-  if (PHASE == 2) pdl_wait();  // phase 1's activations
   const int g = lane >> 2, c = lane & 3;
   const int tid = threadIdx.x;
-  const uint16_t *act = static_cast<const uint16_t *>(P.act);
   uint32_t it = 0;
   uint32_t ep = 0;  // (item, token group)s handed to the epilogue warp
   bool aborted = false;
-
-  // activation row of this lane's token in each N tile (-1: none)
-  auto rows_of = [&](const Cursor &q, int (&arow)[NT]) {
-    const int m_left = q.sg.m - q.grp * TOK;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int col = nt * 8 + g;
-      arow[nt] = -1;
-      if (col < m_left) {
-        const int slot = T.slot(q.sg, q.grp * TOK + col);
-        arow[nt] = PHASE == 1 ? T.token(slot) : slot;
-      }
-    }
-  };
-  // B fragments (this lane's token, the warp's columns of stage q, in the
-  // order of the thread's weight bytes) and the stage's block scales
-  auto load_inputs = [&](const Cursor &q, const int (&arow)[NT], uint32_t (&bfr)[NT][BW],
-                         float &sc_a, float &sc_b) {
-    const int kb0 = q.ks * KBYTES + warp * 64;
-    const bool active = kb0 < kbytes;
-    const int kcol0 = kb0 / ES;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int v = 0; v < BW; ++v) bfr[nt][v] = 0u;
-      if (active && arow[nt] >= 0) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            act + int64_t(arow[nt]) * P.kdim + kcol0 + (FP8 ? 16 * c : 8 * c));
-#pragma unroll
-        for (int v = 0; v < BW / 4; ++v) {
-          const uint4 x = __ldg(src + v);
-          bfr[nt][4 * v + 0] = x.x;
-          bfr[nt][4 * v + 1] = x.y;
-          bfr[nt][4 * v + 2] = x.z;
-          bfr[nt][4 * v + 3] = x.w;
-        }
-      }
-    }
-    sc_a = sc_b = 1.f;
-    if (FP8 && active) {
-      const float *scales =
-          q.sg.expert >= 0 ? P.sc + int64_t(q.sg.expert) * scale_stride : P.sc_sh;
-      const int srow_a = PHASE == 1 ? (q.rb * 32) / 128 : (q.rb * ROWS) / 128;
-      const int srow_b = PHASE == 1 ? (P.inter + q.rb * 32) / 128 : srow_a;
-      sc_a = __ldg(scales + int64_t(srow_a) * scale_cols + kcol0 / 128);
-      sc_b = __ldg(scales + int64_t(srow_b) * scale_cols + kcol0 / 128);
-    }
-  };
 
   float acc[4][NT][4];
 #pragma unroll
@@ -529,31 +553,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   Cursor cur;
   cur.item = blockIdx.x;
   bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, tid == 0);
-  int arow[NT];
-  uint32_t bfr[NT][BW];
-  float sc_a = 1.f, sc_b = 1.f;
-  if (have) {
-    rows_of(cur, arow);
-    load_inputs(cur, arow, bfr, sc_a, sc_b);
-  }
 
   while (have) {
-    // prefetch the next stage's activations and scales
-    Cursor nxt = cur;
-    const bool have_next =
-        cursor_next<TOK>(nxt, T, P.row_blocks, kstages, await_tables, P.err, tid == 0);
-    int arow_n[NT];
-    uint32_t bfr_n[NT][BW];
-    float sc_an = 1.f, sc_bn = 1.f;
-    if (have_next) {
-      if (nxt.ks == 0) rows_of(nxt, arow_n);
-      else {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) arow_n[nt] = arow[nt];
-      }
-      load_inputs(nxt, arow_n, bfr_n, sc_an, sc_bn);
-    }
-
     const int s = it % S;
     const uint32_t round = it / S;
     const int m_left = cur.sg.m - cur.grp * TOK;
@@ -564,24 +565,50 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       s_abort = 1;
       if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
     }
-    if (BF16_ACT_TO_F16) {
-      // the hidden states arrive as bf16 (loaded a stage ago); the fp16 MMA
-      // wants fp16 pairs
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int v = 0; v < BW; ++v) {
-          const uint32_t x = bfr[nt][v];
-          const __half2 h2 =
-              __floats2half2_rn(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-          bfr[nt][v] = *reinterpret_cast<const uint32_t *>(&h2);
-        }
-    }
     if (!aborted && active) {
+      const uint8_t *slot = ring + s * SLOT;
+      // B fragments: this lane's token (row g of each N tile) at the warp's
+      // columns of the stage, in the order of the thread's weight bytes
+      uint32_t bfr[NT][BW];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            slot + ACT_OFF + (nt * 8 + g) * ACT_ROW + (warp * 64 / ES + (FP8 ? 16 * c : 8 * c)) * 2);
+#pragma unroll
+        for (int v = 0; v < BW / 4; ++v) {
+          const uint4 x = src[v];
+          bfr[nt][4 * v + 0] = x.x;
+          bfr[nt][4 * v + 1] = x.y;
+          bfr[nt][4 * v + 2] = x.z;
+          bfr[nt][4 * v + 3] = x.w;
+        }
+      }
+      if (BF16_ACT_TO_F16) {
+        // the hidden states arrive as bf16; the fp16 MMA wants fp16 pairs
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int v = 0; v < BW; ++v) {
+            const uint32_t x = bfr[nt][v];
+            const __half2 h2 =
+                __floats2half2_rn(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+            bfr[nt][v] = *reinterpret_cast<const uint32_t *>(&h2);
+          }
+      }
+      // the block scales of the warp's 64 columns (one 128-column block),
+      // behind the tile: the gate rows' and the up rows' (phase 1), or the
+      // rows' (phase 2)
+      float sc_a = 1.f, sc_b = 1.f;
+      if constexpr (FP8) {
+        const float *sc = reinterpret_cast<const float *>(slot + ROWS * min(KBYTES, kbytes - cur.ks * KBYTES));
+        const int col = warp * 64 / 128;
+        sc_a = sc[col];
+        sc_b = PHASE == 1 ? sc[4 + col] : sc_a;
+      }
       // this warp's 4 KB of the stage: [row tile mt][half h][lane][16 bytes];
       // all of it first, then the MMAs with the four row tiles' chains
       // interleaved (consecutive MMAs are independent)
-      const uint4 *st = reinterpret_cast<const uint4 *>(ring + s * STAGE_BYTES) + warp * 256 + lane;
+      const uint4 *st = reinterpret_cast<const uint4 *>(slot) + warp * 256 + lane;
       uint32_t wl[4][4], wh[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
@@ -668,23 +695,16 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
           for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
     }
 
-    cur = nxt;
-    have = have_next;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      arow[nt] = arow_n[nt];
-#pragma unroll
-      for (int v = 0; v < BW; ++v) bfr[nt][v] = bfr_n[nt][v];
-    }
-    sc_a = sc_an;
-    sc_b = sc_bn;
+    have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, await_tables, P.err, tid == 0);
   }
 }
 
 template <bool FP8, int PHASE, int NT>
 cudaError_t launch_one(const TcParams &P, int grid, cudaStream_t stream) {
   auto kern = expert_tc_kernel<FP8, PHASE, NT>;
-  const size_t smem = smem_bytes<NT>();
+  constexpr size_t smem = smem_bytes<FP8, NT>();
+  // 227 KB per CTA, of which the static plan tables take under 6.5 KB
+  static_assert(smem + 6656 <= 232448, "the ring does not fit in shared memory");
   // the shared-memory opt-in is set once per device (the first call), so
   // later calls, e.g. under stream capture, only launch
   static unsigned long long configured = 0;

@@ -35,9 +35,7 @@ struct TcParams {
   SegTables T;
   const uint8_t *w;       // routed experts' matrix (W13 or W2), expert-major
   const uint8_t *w_sh;    // the shared expert's matrix, or null
-  const float *sc;        // E4M3 block scales of `w` ([N][rows/128][kdim/128])
-  const float *sc_sh;     // E4M3 block scales of `w_sh`
-  int64_t expert_stride;  // bytes between consecutive experts in `w`
+  int64_t expert_stride;  // bytes between consecutive experts in `w` (packed)
   int32_t rows_total;     // rows of one expert's matrix: 2I (phase 1) or d (phase 2)
   int32_t kdim;           // columns: d (phase 1) or I (phase 2)
   int32_t inter;          // I
@@ -73,9 +71,11 @@ cudaError_t launch_expert_f32(int phase, const F32Params &P, int grid, cudaStrea
 
 // Repacks n_matrices expert matrices (rows x kbytes, row-major) into the
 // tile layout of the tensor-core kernel (pack.cu); gate_up selects the W13
-// row order (gate rows, then the matching up rows, per tile).
-cudaError_t launch_pack(const void *src, void *dst, int n_matrices, int rows, int kbytes, int inter,
-                        bool gate_up, cudaStream_t stream);
+// row order (gate rows, then the matching up rows, per tile).  With E4M3
+// block scales ([n_matrices][rows/128][kbytes/128]; else NULL) every tile is
+// followed by its own.
+cudaError_t launch_pack(const void *src, const float *scales, void *dst, int n_matrices, int rows,
+                        int kbytes, int inter, bool gate_up, cudaStream_t stream);
 
 // Router scores logits[t][e] = W_g[e] . h[t] (fp32 accumulation).
 cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h, int n, int d,

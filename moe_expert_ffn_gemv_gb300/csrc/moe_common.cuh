@@ -15,8 +15,18 @@ namespace moe {
 
 // Geometry of a packed weight tile (pack.cu) = one pipeline stage of the
 // tensor-core expert kernel: 64 rows x 512 bytes, 8 consumer warps x 64 bytes.
+// An E4M3 tile is followed by its block scales: 8 floats, the 4 128-column
+// blocks of its first 32 rows, then those of its last 32 rows (W13: gate,
+// then up rows; W2: one 128-row block, so the two halves are equal).
 constexpr int PACK_ROWS = 64;
 constexpr int PACK_KBYTES = 512;
+constexpr int PACK_SCALE_BYTES = 32;
+
+// Packed bytes of one expert matrix of `rows` rows and `kbytes` bytes a row.
+inline int64_t packed_matrix_bytes(int rows, int kbytes, bool fp8) {
+  const int64_t tiles = int64_t(rows / PACK_ROWS) * ((kbytes + PACK_KBYTES - 1) / PACK_KBYTES);
+  return int64_t(rows) * kbytes + (fp8 ? tiles * PACK_SCALE_BYTES : 0);
+}
 
 // ------------------------------------------------------------------ status
 
@@ -81,6 +91,15 @@ __device__ __forceinline__ void fence_barrier_init() {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Raises the transaction count of the current phase of `bar` by `bytes`
+// without arriving (the arrival comes later, with the rest of the phase's
+// copies).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
 }

@@ -61,6 +61,19 @@ def test_expert_bytes_through_the_abi(lib):
     assert lib.moe_expert_bytes(d) == (9_437_184, 0)
 
 
+def test_packed_bytes_through_the_abi(lib):
+    # DeepSeek-V3 FP8: W13 2I x d = 4096 x 7168 bytes in 64 x 14 tiles of 64 rows x 512 bytes,
+    # W2 d x I = 7168 x 2048 bytes in 112 x 4 tiles; each tile carries 32 bytes of scales
+    assert lib.moe_packed_bytes(_desc(lib)) == (4096 * 7168 + 64 * 14 * 32,
+                                                7168 * 2048 + 112 * 4 * 32)
+    # a ragged E4M3 shape: K = 640 bytes is 2 tiles a row block, K = 384 one
+    assert lib.moe_packed_bytes(_desc(lib, d=640, inter=384)) == (768 * 640 + 12 * 2 * 32,
+                                                                 640 * 384 + 10 * 1 * 32)
+    # bf16: the row-major size
+    d = _desc(lib, d=2048, n_experts=128, inter=768, n_shared=0, w_dtype=lib.MOE_BF16)
+    assert lib.moe_packed_bytes(d) == (2 * 768 * 2048 * 2, 2048 * 768 * 2)
+
+
 def test_workspace_bytes_and_desc_checks(lib):
     assert lib.moe_workspace_bytes(_desc(lib)) > 0
     bad = [dict(d=0), dict(top_k=0), dict(top_k=300), dict(n_experts=-1), dict(n_shared=-1),
@@ -89,18 +102,20 @@ def test_launching_calls_reject_bad_arguments_before_any_launch(lib):
     y = P(0x1000)
     assert r.moe_route_topk(ctypes.byref(D), y, y, 65, y, y, y, s0) == lib.MOE_ERR_INVALID_ARG
     assert r.moe_topk_from_logits(ctypes.byref(D), y, -1, y, y, s0) == lib.MOE_ERR_INVALID_ARG
-    W = lib.moe_expert_weights(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    W = lib.moe_expert_weights(0x1000, 0x1000, 0x1000, 0x1000)
     plan = lib.moe_plan(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
     nb = lib.moe_workspace_bytes(D)
     # workspace too small
     assert r.moe_verify_dedup(ctypes.byref(D), ctypes.byref(W), y, 8, y, y, ctypes.byref(plan), y,
                               nb - 1, y, s0) == lib.MOE_ERR_WORKSPACE
-    # missing scales for E4M3 weights
-    W2 = lib.moe_expert_weights(0x1000, 0x1000, None, None, 0x1000, 0x1000, 0x1000, 0x1000)
-    assert r.moe_verify_perslot(ctypes.byref(D), ctypes.byref(W2), y, 8, y, y, y, nb, y,
-                                s0) == lib.MOE_ERR_INVALID_ARG
+    # E4M3 weights packed without their scales
+    z = P(0x2000)
+    assert r.moe_pack_expert_weights(ctypes.byref(D), y, y, None, None, 2, z, z,
+                                     s0) == lib.MOE_ERR_INVALID_ARG
+    assert r.moe_pack_expert_weights(ctypes.byref(D), y, y, x, y, 2, z, z,
+                                     s0) == lib.MOE_ERR_ALIGNMENT
     # missing shared expert when the desc has one
-    W3 = lib.moe_expert_weights(0x1000, 0x1000, 0x1000, 0x1000, None, None, None, None)
+    W3 = lib.moe_expert_weights(0x1000, 0x1000, None, None)
     assert r.moe_verify_perslot(ctypes.byref(D), ctypes.byref(W3), y, 8, y, y, y, nb, y,
                                 s0) == lib.MOE_ERR_INVALID_ARG
     # plan without arrays

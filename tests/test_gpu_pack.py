@@ -1,5 +1,6 @@
-"""moe_pack_expert_weights writes the tile layout include/moe_verify.h states,
-checked piece by piece against a numpy transcription of that statement."""
+"""moe_pack_expert_weights writes the tile layout include/moe_verify.h states
+(E4M3: each tile followed by its 8 block scales), checked piece by piece
+against a numpy transcription of that statement."""
 import numpy as np
 import pytest
 import torch
@@ -15,10 +16,12 @@ def mv():
     return binding
 
 
-def expected_packed(mat: np.ndarray, gate_up: bool, inter: int) -> np.ndarray:
-    """mat: one expert matrix as uint8 [rows][K bytes] -> packed bytes."""
+def expected_packed(mat: np.ndarray, gate_up: bool, inter: int, scales=None) -> np.ndarray:
+    """mat: one expert matrix as uint8 [rows][K bytes] -> packed bytes; scales:
+    its E4M3 block scales [rows/128][K/128] (float32) or None."""
     rows, K = mat.shape
-    out = np.empty(rows * K, dtype=np.uint8)
+    tiles = (rows // 64) * ((K + 511) // 512)
+    out = np.empty(rows * K + (32 * tiles if scales is not None else 0), dtype=np.uint8)
     pos = 0
     for rb in range(rows // 64):
         for kc in range((K + 511) // 512):
@@ -35,7 +38,19 @@ def expected_packed(mat: np.ndarray, gate_up: bool, inter: int) -> np.ndarray:
                             col = 512 * kc + 64 * w + 16 * (lane % 4)
                             out[pos:pos + 16] = mat[row, col:col + 16]
                             pos += 16
-    assert pos == rows * K
+            if scales is not None:
+                # the 128-row blocks of the tile's first and last 32 rows
+                blocks = ((32 * rb) // 128, (inter + 32 * rb) // 128) if gate_up else \
+                    ((64 * rb) // 128,) * 2
+                tr = np.zeros(8, dtype=np.float32)
+                for half, br in enumerate(blocks):
+                    for t in range(4):
+                        c = 4 * kc + t
+                        if c < scales.shape[1]:
+                            tr[4 * half + t] = scales[br, c]
+                out[pos:pos + 32] = tr.view(np.uint8)
+                pos += 32
+    assert pos == out.size
     return out
 
 
@@ -48,13 +63,17 @@ def test_pack_layout(mv, wtype, d, inter):
     packed = mv.pack_weights(layer, desc)
     torch.cuda.synchronize()
     es = 1 if wtype == synth.E4M3 else 2
+    b13, b2 = mv.moe_packed_bytes(desc)
+    fp8 = wtype == synth.E4M3
     for e in range(cfg.n_experts):
-        for src, dst, gate_up in ((layer.w13[e], packed.w13[e], True),
-                                  (layer.w2[e], packed.w2[e], False)):
+        for src, dst, sc, gate_up in (
+                (layer.w13[e], packed.w13[e * b13:(e + 1) * b13], layer.s13, True),
+                (layer.w2[e], packed.w2[e * b2:(e + 1) * b2], layer.s2, False)):
             m = src.contiguous().view(torch.uint8).cpu().numpy().reshape(src.shape[0], -1)
             assert m.shape[1] == src.shape[1] * es
-            got = dst.contiguous().view(torch.uint8).cpu().numpy().ravel()
-            assert np.array_equal(got, expected_packed(m, gate_up, inter))
+            got = dst.cpu().numpy()
+            scales = sc[e].cpu().numpy() if fp8 else None
+            assert np.array_equal(got, expected_packed(m, gate_up, inter, scales))
 
 
 def test_pack_fp32_is_a_copy(mv):
@@ -62,4 +81,5 @@ def test_pack_fp32_is_a_copy(mv):
     layer = synth.make_layer(cfg, device="cuda")
     packed = mv.pack_weights(layer, mv.make_desc(cfg, 2))
     torch.cuda.synchronize()
-    assert torch.equal(packed.w13, layer.w13) and torch.equal(packed.w2, layer.w2)
+    assert torch.equal(packed.w13, layer.w13.contiguous().view(torch.uint8).ravel())
+    assert torch.equal(packed.w2, layer.w2.contiguous().view(torch.uint8).ravel())

@@ -58,7 +58,7 @@ def test_noalloc_rejects_a_call_beyond_its_fixed_scratch(mv):
     # DeepSeek-V3 shapes: 64 tokens x 9 slots need about 19 MB of scratch
     desc = mv.make_desc(synth.DSV3, 64)
     fake = 0x10000  # never dereferenced: the size check comes before any launch
-    W = mv.moe_expert_weights(fake, fake, fake, fake, fake, fake, fake, fake)
+    W = mv.moe_expert_weights(fake, fake, fake, fake)
     plan = mv.moe_plan(fake, fake, fake, fake, fake, fake)
     p = ctypes.c_void_p(fake)
     st = mv._lib.moe_verify_dedup_noalloc(ctypes.byref(desc), ctypes.byref(W), p, 64, p, p,
