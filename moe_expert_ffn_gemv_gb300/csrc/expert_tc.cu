@@ -19,15 +19,15 @@
 //     one pipeline stage form one contiguous tile, its 16-byte pieces in the
 //     order the consumer threads read them, an E4M3 tile followed by its 8
 //     block scales;
-//   - warp 8 is the producer: per stage it fills one slot of a 5-stage
-//     shared-memory ring with a 1-D TMA bulk copy (cp.async.bulk, completing
-//     on the slot's mbarrier) of the tile and its scales, and one bulk copy
-//     per token of the K chunk of that token's activation row.  So the
+//   - two producer warps fill each slot of a 5-stage shared-memory ring,
+//     both completing on the slot's mbarrier: warp 8 with one 1-D TMA bulk
+//     copy (cp.async.bulk) of the tile and its scales, warp 10 with one bulk
+//     copy per token of the K chunk of that token's activation row.  So the
 //     consumers read nothing but shared memory: a global load issued by a
 //     consumer returns behind the SM's stream of weight tiles, several
-//     stages late, and stalls it.  The producer's issue time per copy is
-//     what keeps it from running further ahead, so a stage costs it as few
-//     copies as possible (no separate scale copy);
+//     stages late, and stalls it.  A warp's issue time per copy is what
+//     keeps it from running further ahead, hence one copy a stage for the
+//     weight stream (no separate scale copy; the rows on their own warp);
 //   - warps 0..7 consume: warp w owns bytes [64 w, 64 w + 64) of every row of a
 //     stage, i.e. a K-split across warps, and runs mma.sync m16n8k16 with the
 //     weights as the 16-row A operand (4 row tiles) and the segment's tokens as
@@ -60,9 +60,10 @@ constexpr int ROWS = PACK_ROWS;      // weight rows per stage (4 MMA row tiles)
 constexpr int KBYTES = PACK_KBYTES;  // bytes of each row per stage
 constexpr int STAGE_BYTES = ROWS * KBYTES;
 constexpr int CONSUMERS = 8;                      // warps 0..7
-constexpr int PRODUCER = CONSUMERS;                // warp 8
+constexpr int PRODUCER = CONSUMERS;                // warp 8: weight tiles
 constexpr int EPILOGUE = CONSUMERS + 1;            // warp 9
-constexpr int THREADS = (CONSUMERS + 2) * 32;
+constexpr int ACTS = CONSUMERS + 2;                // warp 10: activation rows
+constexpr int THREADS = (CONSUMERS + 3) * 32;
 constexpr uint64_t DRAIN_LIMIT_NS = 200ull * 1000 * 1000;
 
 // Shared memory: a ring of S slots, each with one stage's weight tile (E4M3:
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // the tile's and the activations' producers
       mbar_init(&empty[s], CONSUMERS);
     }
     for (int b = 0; b < RB; ++b) {
@@ -442,55 +443,22 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       plan_ready = true;
       return true;
     };
-    // Fills slot s with stage q: the packed tile of (row block, K chunk),
-    // contiguous, ROWS * nb bytes of weights followed (E4M3) by the tile's
-    // block scales (weights); the K chunk of each of the stage's tokens'
-    // activation rows, one bulk copy per row (acts).  The barrier's phase
-    // closes (the producer's arrival) with the activations: before them
-    // only the tile's bytes are announced.  The consumers read nothing but
-    // shared memory (a global load of theirs would come back behind the
-    // SM's stream of weight tiles), and the producer issues as few copies
-    // as it can: each costs it issue time, and it must keep ahead of HBM.
-    const uint8_t *act = static_cast<const uint8_t *>(P.act);
-    auto issue_stage = [&](const Cursor &q, int s, bool weights, bool acts) {
-      uint8_t *slot = ring + s * SLOT;
-      const int k0 = q.ks * KBYTES;
-      const int nb = min(KBYTES, kbytes - k0);
+    // Stage q's packed tile of (row block, K chunk) into slot s: contiguous,
+    // ROWS * nb bytes of weights followed (E4M3) by the tile's block scales,
+    // one bulk copy.  The copy issue time of this warp bounds how far ahead
+    // of HBM it can run, hence a single copy a stage (the scales packed into
+    // the tile, the activation rows left to their own warp).
+    auto issue_tile = [&](const Cursor &q, int s) {
+      const int nb = min(KBYTES, kbytes - q.ks * KBYTES);
       const uint32_t tile_bytes = uint32_t(ROWS * nb + TRAILER);
-      const uint32_t row_bytes = uint32_t(nb / ES) * 2;
-      const int m_rows = acts ? max(0, min(TOK, q.sg.m - q.grp * TOK)) : 0;
       if (lane == 0) {
-        const uint32_t tx = (weights ? tile_bytes : 0u) + uint32_t(m_rows) * row_bytes;
-        if (acts) mbar_arrive_expect_tx(&full[s], tx);
-        else mbar_expect_tx(&full[s], tx);
-      }
-      __syncwarp();
-      if (weights && lane == 0) {
+        mbar_arrive_expect_tx(&full[s], tile_bytes);
         const uint8_t *base =
             q.sg.expert >= 0 ? P.w + int64_t(q.sg.expert) * P.expert_stride : P.w_sh;
-        bulk_g2s(slot, base + q.rb * rb_bytes + int64_t(q.ks) * (ROWS * KBYTES + TRAILER),
+        bulk_g2s(ring + s * SLOT, base + q.rb * rb_bytes + int64_t(q.ks) * (ROWS * KBYTES + TRAILER),
                  tile_bytes, &full[s], q.sg.expert >= 0 && q.grp + 1 < q.groups ? keep : policy);
       }
-      for (int j = lane; j < m_rows; j += 32) {
-        const int sl = T.slot(q.sg, q.grp * TOK + j);
-        const int row = PHASE == 1 ? T.token(sl) : sl;
-        bulk_g2s(slot + ACT_OFF + j * ACT_ROW, act + (int64_t(row) * P.kdim + k0 / ES) * 2,
-                 row_bytes, &full[s], keep);
-      }
-    };
-    // Phase 2: the activations of the stages issued so far (at most S),
-    // once phase 1 has ended.
-    bool acts_ok = PHASE == 1;
-    auto late_acts = [&]() {
-      pdl_wait();
-      Cursor q;
-      q.item = blockIdx.x;
-      bool h = cursor_item<TOK>(q, T, P.row_blocks, load_plan, P.err, false);
-      for (uint32_t j = 0; j < it && h; ++j) {
-        issue_stage(q, int(j), false, true);
-        h = cursor_next<TOK>(q, T, P.row_blocks, kstages, load_plan, P.err, false);
-      }
-      acts_ok = true;
+      __syncwarp();
     };
     Cursor cur;
     cur.item = blockIdx.x;
@@ -503,9 +471,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
         break;
       }
       if (s_abort) { ok = false; break; }
-      issue_stage(cur, s, true, acts_ok);
+      issue_tile(cur, s);
       ++it;
-      if (!acts_ok && it == uint32_t(S)) late_acts();
       if (plan_ready && !joined && ++since_plan >= S) {
         // the ring is full: wait for the plan kernel's end, then let phase 2 launch
         pdl_wait();
@@ -514,10 +481,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
       have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, load_plan, P.err, false);
     }
-    // Phase 1 must not end before the plan kernel, whatever path led here;
-    // phase 2 closes the stages still waiting for their activations.
+    // Phase 1 must not end before the plan kernel, whatever path led here.
     if (!joined) pdl_wait();
-    if (!acts_ok) late_acts();
     if (!ok) {
       if (lane == 0) {
         record_error(P.err, MOE_ERR_TIMEOUT);
@@ -528,6 +493,59 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     const uint32_t issued = it;
     const uint32_t first = issued > uint32_t(S) ? issued - S : 0;
     for (uint32_t j = first; j < issued; ++j)
+      if (!mbar_wait_bounded(&full[j % S], (j / S) & 1, DRAIN_LIMIT_NS)) {
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+        break;
+      }
+    return;
+  }
+
+  if (warp == ACTS) {
+    // ---------------------------------------------------- activation rows
+    // For each stage, the K chunk of each of its tokens' activation rows,
+    // one bulk copy per row into the slot, behind the slot's tile: the
+    // consumers then read nothing but shared memory (a global load of
+    // theirs would come back behind the SM's stream of weight tiles,
+    // several stages late).  Phase 2 reads phase 1's activations, so it
+    // waits for phase 1 to end first; its weight tiles stream meanwhile.
+    if (PHASE == 2) pdl_wait();
+    const uint64_t keep = policy_evict_normal();
+    const uint8_t *act = static_cast<const uint8_t *>(P.act);
+    uint32_t it = 0;
+    bool ok = true;
+    Cursor cur;
+    cur.item = blockIdx.x;
+    bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
+    while (have) {
+      const int s = it % S;
+      const uint32_t round = it / S;
+      if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1, P.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      if (s_abort) break;
+      const int k0 = cur.ks * KBYTES;
+      const uint32_t row_bytes = uint32_t(min(KBYTES, kbytes - k0) / ES) * 2;
+      const int m_rows = max(0, min(TOK, cur.sg.m - cur.grp * TOK));
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], uint32_t(m_rows) * row_bytes);
+      __syncwarp();
+      for (int j = lane; j < m_rows; j += 32) {
+        const int sl = T.slot(cur.sg, cur.grp * TOK + j);
+        const int row = PHASE == 1 ? T.token(sl) : sl;
+        bulk_g2s(ring + s * SLOT + ACT_OFF + j * ACT_ROW,
+                 act + (int64_t(row) * P.kdim + k0 / ES) * 2, row_bytes, &full[s], keep);
+      }
+      __syncwarp();
+      ++it;
+      have = cursor_next<TOK>(cur, T, P.row_blocks, kstages, await_tables, P.err, false);
+    }
+    if (!ok && lane == 0) {
+      record_error(P.err, MOE_ERR_TIMEOUT);
+      s_abort = 1;
+    }
+    // Let every copy this warp issued land before the CTA may exit.
+    const uint32_t first = it > uint32_t(S) ? it - S : 0;
+    for (uint32_t j = first; j < it; ++j)
       if (!mbar_wait_bounded(&full[j % S], (j / S) & 1, DRAIN_LIMIT_NS)) {
         if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
         break;
