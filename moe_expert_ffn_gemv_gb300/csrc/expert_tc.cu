@@ -65,6 +65,11 @@ constexpr int EPILOGUE = CONSUMERS + 1;            // warp 9
 constexpr int ACTS = CONSUMERS + 2;                // warp 10: activation rows
 constexpr int THREADS = (CONSUMERS + 3) * 32;
 constexpr uint64_t DRAIN_LIMIT_NS = 200ull * 1000 * 1000;
+// Phase 2: stages past the first S that each CTA prefetches into L2 once its
+// ring is full.  Phase 2's CTAs start as phase 1's finish, and phase 1's
+// last CTAs end some 15 us after the median one: the prefetch puts the HBM
+// bandwidth they leave idle to use (-4 us on the n = 8 pass).
+constexpr int PREFETCH_AHEAD = 8;
 
 // Shared memory: a ring of S slots, each with one stage's weight tile (E4M3:
 // with its 8 block scales behind it) and the activation rows of its tokens;
@@ -460,6 +465,23 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
       __syncwarp();
     };
+    // The tiles of the next `stages` stages from q into L2 (one prefetch per
+    // item: an item's tiles are contiguous).
+    auto prefetch_stages = [&](Cursor q, int stages) {
+      bool h = true;
+      while (h && stages > 0) {
+        const int n = min(stages, kstages - q.ks);
+        const uint8_t *base =
+            q.sg.expert >= 0 ? P.w + int64_t(q.sg.expert) * P.expert_stride : P.w_sh;
+        const int64_t off = q.rb * rb_bytes + int64_t(q.ks) * (ROWS * KBYTES + TRAILER);
+        const int64_t end = q.ks + n == kstages ? (q.rb + 1) * rb_bytes
+                                                : off + int64_t(n) * (ROWS * KBYTES + TRAILER);
+        if (lane == 0) prefetch_l2(base + off, uint64_t(end - off));
+        stages -= n;
+        q.ks += n - 1;
+        h = cursor_next<TOK>(q, T, P.row_blocks, kstages, load_plan, P.err, false);
+      }
+    };
     Cursor cur;
     cur.item = blockIdx.x;
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, load_plan, P.err, false);
@@ -473,6 +495,11 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       if (s_abort) { ok = false; break; }
       issue_tile(cur, s);
       ++it;
+      if (PHASE == 2 && PREFETCH_AHEAD > 0 && it == uint32_t(S)) {
+        Cursor q = cur;
+        if (cursor_next<TOK>(q, T, P.row_blocks, kstages, load_plan, P.err, false))
+          prefetch_stages(q, PREFETCH_AHEAD);
+      }
       if (plan_ready && !joined && ++since_plan >= S) {
         // the ring is full: wait for the plan kernel's end, then let phase 2 launch
         pdl_wait();

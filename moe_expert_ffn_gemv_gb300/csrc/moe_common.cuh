@@ -154,6 +154,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Asks L2 to fetch [p, p + bytes) ahead of use, at normal priority (a hint;
+// p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint64_t bytes) {
+  const char *c = static_cast<const char *>(p);
+  while (bytes > 0) {
+    const uint32_t n = uint32_t(bytes < (1u << 20) ? bytes : (1u << 20));
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(n) : "memory");
+    c += n;
+    bytes -= n;
+  }
+}
+
 // ------------------------------------------------------------ tensor cores
 
 // D += A * B for one m16n8k16 tile, f16 or bf16 inputs, fp32 accumulators.
