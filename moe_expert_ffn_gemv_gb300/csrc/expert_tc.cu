@@ -165,12 +165,27 @@ struct LocalTables {
   __device__ int token(int slot) const { return slot < n * k ? slot / k : slot - n * k; }
 };
 
-// Position in the (item, token group, K stage) sequence a CTA walks.  The
-// producer and all consumer warps walk the same sequence.
+// Position in the (work item, K stage) sequence a CTA walks; the producer,
+// activation, consumer and epilogue warps all walk the same sequence.  A
+// work item is (segment, row block, token group of TOK tokens); items are
+// numbered segment by segment, row block by row block, the token group
+// innermost, and CTA b takes items b, b + gridDim.x, ...  A segment of more
+// than TOK tokens (the shared expert at n > 8, a popular routed expert) thus
+// spreads its groups over consecutive CTAs, which balances the CTAs' work
+// and has them read the same tiles at about the same time (L2 hits after
+// the first).
 struct Cursor {
   int item, rb, grp, ks, groups;
+  int u, seg_first, seg_items;  // segment, its first item, its items
   Seg sg;
 };
+
+__device__ __forceinline__ void cursor_start(Cursor &c) {
+  c.item = blockIdx.x;
+  c.u = -1;
+  c.seg_first = 0;
+  c.seg_items = 0;
+}
 
 // ensure() makes the plan's tables usable (it may wait for them) and
 // returns false when the kernel must stop.
@@ -178,21 +193,27 @@ template <int TOK, typename Ensure>
 __device__ __forceinline__ bool cursor_item(Cursor &c, const LocalTables &T, int row_blocks,
                                             Ensure &ensure, int32_t *err, bool report) {
   for (;;) {
-    const int u = c.item / row_blocks;
-    if (u >= T.plan_free_segments()) {
-      if (!ensure()) return false;
-      if (u >= T.n_segments()) return false;
-    }
-    c.rb = c.item - u * row_blocks;
-    c.sg = T.segment(u);
-    if (c.sg.expert != -2) {
-      c.groups = (c.sg.m + TOK - 1) / TOK;
-      c.grp = 0;
+    if (c.item < c.seg_first + c.seg_items) {
+      const int j = c.item - c.seg_first;
+      c.rb = j / c.groups;
+      c.grp = j - c.rb * c.groups;
       c.ks = 0;
       return true;
     }
-    if (report && c.rb == 0) record_error(err, MOE_ERR_DEVICE_INPUT);
-    c.item += gridDim.x;
+    c.seg_first += c.seg_items;
+    c.u += 1;
+    if (c.u >= T.plan_free_segments()) {
+      if (!ensure()) return false;
+      if (c.u >= T.n_segments()) return false;
+    }
+    c.sg = T.segment(c.u);
+    if (c.sg.expert == -2) {
+      if (report) record_error(err, MOE_ERR_DEVICE_INPUT);
+      c.seg_items = 0;
+      continue;
+    }
+    c.groups = (c.sg.m + TOK - 1) / TOK;
+    c.seg_items = row_blocks * c.groups;
   }
 }
 
@@ -201,8 +222,6 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
                                             int kstages, Ensure &ensure, int32_t *err,
                                             bool report) {
   if (++c.ks < kstages) return true;
-  c.ks = 0;
-  if (++c.grp < c.groups) return true;
   c.item += gridDim.x;
   return cursor_item<TOK>(c, T, row_blocks, ensure, err, report);
 }
@@ -344,7 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     bool aborted = false;
     uint32_t ep = 0;
     Cursor cur;
-    cur.item = blockIdx.x;
+    cursor_start(cur);
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
     while (have) {
       const int b = ep % RB;
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
     };
     Cursor cur;
-    cur.item = blockIdx.x;
+    cursor_start(cur);
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, load_plan, P.err, false);
     while (have) {
       const int s = it % S;
@@ -541,7 +560,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     uint32_t it = 0;
     bool ok = true;
     Cursor cur;
-    cur.item = blockIdx.x;
+    cursor_start(cur);
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
     while (have) {
       const int s = it % S;
@@ -596,7 +615,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
 
   Cursor cur;
-  cur.item = blockIdx.x;
+  cursor_start(cur);
   bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, tid == 0);
 
   while (have) {
