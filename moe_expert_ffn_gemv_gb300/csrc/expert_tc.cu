@@ -67,8 +67,10 @@ constexpr int THREADS = (CONSUMERS + 3) * 32;
 constexpr uint64_t DRAIN_LIMIT_NS = 200ull * 1000 * 1000;
 // Phase 2: stages past the first S that each CTA prefetches into L2 once its
 // ring is full.  Phase 2's CTAs start as phase 1's finish, and phase 1's
-// last CTAs end some 15 us after the median one: the prefetch puts the HBM
-// bandwidth they leave idle to use (-4 us on the n = 8 pass).
+// last CTAs end some 9 us after the median one: the prefetch puts the HBM
+// bandwidth they leave idle to use (-4 us on the n = 8 pass).  Passes of
+// fewer than 4 items a CTA leave no such idle time, and there the prefetch
+// only delays the copies queued behind it, so it is skipped.
 constexpr int PREFETCH_AHEAD = 8;
 
 // Shared memory: a ring of S slots, each with one stage's weight tile (E4M3:
@@ -514,7 +516,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       if (s_abort) { ok = false; break; }
       issue_tile(cur, s);
       ++it;
-      if (PHASE == 2 && PREFETCH_AHEAD > 0 && it == uint32_t(S)) {
+      if (PHASE == 2 && PREFETCH_AHEAD > 0 && it == uint32_t(S) &&
+          T.n_segments() * P.row_blocks >= 4 * int(gridDim.x)) {
         Cursor q = cur;
         if (cursor_next<TOK>(q, T, P.row_blocks, kstages, load_plan, P.err, false))
           prefetch_stages(q, PREFETCH_AHEAD);
