@@ -14,7 +14,8 @@
 //   PHASE 2  y_slot = W2 a           over rows [64 rb, 64 rb + 64) of W2, K = I;
 //            writes yslot[slot][d] (fp32).
 //
-// Structure (one CTA per SM, persistent over work items (segment, row block)):
+// Structure (one CTA per SM, persistent over work items (segment, row block,
+// token group of 8 tokens)):
 //   - the weights are stored pre-packed (pack.cu): the 64 rows x 512 bytes of
 //     one pipeline stage form one contiguous tile, its 16-byte pieces in the
 //     order the consumer threads read them, an E4M3 tile followed by its 8
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   //  - Phase 1 of the deduplicating engine with a shared expert, launched
   //    right behind its pass's plan kernel (early_shared; "lazy"): the
   //    shared expert's items need no plan, so the CTAs start on them at
-  //    once.  When its walk leaves the shared segment, the producer warp
+  //    once.  When its walk leaves the shared segment, the weight warp
   //    waits (bounded) for the plan kernel's plan-ready flag, copies the
   //    plan through L2 to shared memory and signals tables_bar, on which
   //    the other warps wait (bounded).  Once the ring is full it also waits
@@ -271,10 +272,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   //    then triggers phase 2, so phase 2 still reads a complete plan, and
   //    phase 1 never ends before the plan kernel.
   //  - Otherwise phase 1 waits for the plan at once; phase 2 reads the plan
-  //    (complete before phase 1 triggered it) at once.  Its producer streams
-  //    the first S stages' weights from the start, behind the end of phase
-  //    1, then waits for phase 1 to end before it copies phase 1's
-  //    activations (and only then closes those stages).
+  //    (complete before phase 1 triggered it) at once.  Phase 2's weight
+  //    warp streams its first S stages' tiles from the start, behind the
+  //    end of phase 1; its activation warp waits for phase 1 to end before
+  //    it copies phase 1's activations, which completes those stages.
   const bool lazy =
       PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared && P.ready != nullptr;
   // via_l2: read through L2 (the plan kernel may still be running)
@@ -427,10 +428,12 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
 
   if (warp == PRODUCER) {
     // ------------------------------------------------------------ producer
-    // A segment with more tokens than one pass takes (the shared expert, a
-    // popular routed expert) streams its item's weights once per group of
-    // TOK tokens: every pass but the last loads them at normal L2 priority,
-    // so that the evict-first stream leaves them for the next pass.
+    // A segment of more than TOK tokens (the shared expert at n > TOK, a
+    // popular routed expert) streams a row block's tiles once per group of
+    // TOK tokens, consecutive work items.  A routed expert's groups before
+    // the last load them at normal L2 priority, so that the evict-first
+    // stream leaves them for the later groups; the shared expert's stay
+    // evict-first (measured faster on DeepSeek-V3 stacks).
     const uint64_t policy = policy_evict_first();
     const uint64_t keep = policy_evict_normal();
     uint32_t it = 0;
