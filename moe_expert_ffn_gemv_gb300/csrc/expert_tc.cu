@@ -278,9 +278,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   //    it copies phase 1's activations, which completes those stages.
   const bool lazy =
       PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared && P.ready != nullptr;
-  // via_l2: read through L2 (the plan kernel may still be running)
-  auto load_tables = [&](int first, int step, bool via_l2) {
-    auto rd = [via_l2](const int32_t *p) { return via_l2 ? __ldcg(p) : *p; };
+  // the plan (or, per-slot, the ids) into shared memory, threads first,
+  // first + step, ... (the early-start mode has its own loader, below)
+  auto load_tables = [&](int first, int step) {
+    auto rd = [](const int32_t *p) { return *p; };
     const int32_t *src = P.T.dedup ? P.T.perm : P.T.ids;
     const int lim = P.T.dedup ? nk : P.T.n_experts;
     for (int i = first; i < nk; i += step) {
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     s_abort = 0;
     fence_barrier_init();
   }
-  if (!lazy) load_tables(threadIdx.x, THREADS, false);
+  if (!lazy) load_tables(threadIdx.x, THREADS);
   __syncthreads();
   if (!lazy && __syncthreads_or(plan_bad(threadIdx.x, THREADS))) {
     if (threadIdx.x == 0) {
@@ -461,7 +462,33 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
         s_abort = 1;
         return false;
       }
-      load_tables(lane, 32, true);
+      // The plan through L2 (its kernel wrote it just now), in as few round
+      // trips as the warp can: U, then the n*k perm entries and the U uniq
+      // and U + 1 offs entries (all the walk reads) as one index space, 8
+      // loads in flight a lane before any store.  Loading every table entry
+      // in lane-strided loops took 2.3-2.9 us here.
+      const int U = __ldcg(P.T.n_uniq);
+      const int Uc = U < 0 ? 0 : U > P.T.n_experts ? P.T.n_experts : U;
+      const int total = nk + Uc + Uc + 1;
+      for (int base = 0; base < total; base += 8 * 32) {
+        int32_t v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = base + q * 32 + lane;
+          const int32_t *src = i < nk        ? P.T.perm + i
+                               : i < nk + Uc ? P.T.uniq + (i - nk)
+                                             : P.T.offs + (i - nk - Uc);
+          v[q] = i < total ? __ldcg(src) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = base + q * 32 + lane;
+          if (i < nk) s_tab[i] = int16_t(v[q] >= 0 && v[q] < nk ? v[q] : -1);
+          else if (i < nk + Uc) s_uniq[i - nk] = v[q];
+          else if (i < total) s_offs[i - nk - Uc] = v[q];
+        }
+      }
+      if (lane == 0) s_U = U;
       __syncwarp();
       if (__any_sync(0xffffffffu, plan_bad(lane, 32)) && lane == 0) {
         s_U = 0;
