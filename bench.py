@@ -52,7 +52,7 @@ def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-sweep", action="store_true", help="skip the n = 1..64 engine sweep")
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
@@ -281,6 +281,19 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = whole_job_gbs(union_bytes, ms_per_step, ws)
 
+    # the spread of single passes: the same graph replayed K more times, each
+    # replay between its own pair of events (outside the timed region above)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        g_pass.replay()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_pass = sorted(1e3 * evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    q = lambda f: per_pass[min(len(per_pass) - 1, int(f * (len(per_pass) - 1) + 0.5))]
+    replays = {"median_us": round(statistics.median(per_pass), 2),
+               "iqr_us": [round(q(0.25), 2), round(q(0.75), 2)], "replays": args.steps}
+
     # algorithmic bytes of one moe_verify_dedup call: union expert bytes + the
     # hidden states (bf16, read once), the intermediate a (fp16, written and
     # read once per slot), the per-slot fp32 outputs (written, read), y (bf16)
@@ -371,6 +384,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (union bytes per pass >> 129 MB), no flush",
                        "parallelism": f"replicas x{ws}"},
             "us_per_pass": round(1e3 * ms_per_step, 2),
+            "us_per_pass_single_replays": replays,
             "us_dedup_call": round(1e3 * dedup_avg, 2),
             "pct_of_nominal_8tbs_whole_pass": round(100 * value / ws / NOMINAL_HBM_GBS, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
