@@ -450,11 +450,19 @@ def engine_sweep(mv, layer, h_all, n_max, eb, reps=5, n_min=1, cfg=None):
         assert vl.last_error() == 0
         raw.append(dict(n=n, U=U, t_dedup=t["dedup"], t_slot=t["perslot"]))
     an = X.analyse(raw, cfg.top_k, eb, cfg.n_shared)
+    # consecutive-token reuse of the window: token n's experts already chosen
+    # by the tokens before it (the routing of a token does not depend on the
+    # pass size, so one routing of the largest pass gives every n)
+    vl.route_plan(h_all[:n_max].contiguous(), n_max)
+    torch.cuda.synchronize()
+    reuse = [None] + X.consecutive_reuse(vl.ids_view(n_max).cpu().tolist())
     rows = [[a_["n"], a_["U"], round(1e6 * a_["t_dedup"], 1), round(1e6 * a_["t_slot"], 1),
              round(a_["u_bar"], 3), round(a_["r"], 3), round(a_["beta_dedup"] / 1e9, 1),
-             round(a_["beta_slot"] / 1e9, 1)] for a_ in an]
+             round(a_["beta_slot"] / 1e9, 1),
+             None if reuse[a_["n"] - 1] is None else round(reuse[a_["n"] - 1], 3),
+             round(X.uniform_reuse(a_["n"], cfg.top_k, cfg.n_experts), 3)] for a_ in an]
     return {"columns": ["n", "U", "us_dedup", "us_perslot", "u_bar", "r", "gbs_dedup_union",
-                        "gbs_perslot_requested"],
+                        "gbs_perslot_requested", "reuse_rho", "reuse_rho_uniform"],
             "rows": rows,
             "crossover_n": X.crossover([a_["n"] for a_ in an], [a_["t_dedup"] for a_ in an],
                                        [a_["t_slot"] for a_ in an]),

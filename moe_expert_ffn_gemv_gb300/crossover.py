@@ -53,6 +53,31 @@ def crossover(ns: Sequence[int], t_dedup: Sequence[float], t_slot: Sequence[floa
     return None
 
 
+def consecutive_reuse(ids: Sequence[Sequence[int]]) -> List[float]:
+    """Consecutive-token reuse of one window of routed tokens, in the pass's
+    token order: entry n - 2 (n = 2 .. len(ids)) is the share of token n's
+    experts that the n - 1 tokens before it already selected ("Speculative
+    Decoding for Mixture-of-Experts Models: Expert Bytes, Kernel Bandwidth
+    and the Best Draft Length", Fig. 1, rho_l(n) of one layer).  The page
+    prints no formula; this reading is the one whose mean under independent
+    uniform routing is the figure's dotted line (uniform_reuse)."""
+    seen = set()
+    out = []
+    for t, row in enumerate(ids):
+        row = list(row)
+        if t > 0:
+            out.append(sum(1 for e in row if e in seen) / len(row))
+        seen.update(row)
+    return out
+
+
+def uniform_reuse(n: int, k: int, n_experts: int) -> float:
+    """Mean consecutive-token reuse under independent uniform routing:
+    1 - q^(n-1) with q = 1 - k/N, the chance that a given expert is missing
+    from one token's k of N (same figure, dotted line)."""
+    return 1.0 - (1.0 - k / n_experts) ** (n - 1)
+
+
 def analyse(rows: Iterable[Dict], k: int, expert_bytes: int, n_shared: int = 0) -> List[Dict]:
     """rows: dicts with n, U, t_dedup, t_slot (seconds) -> adds u_bar, betas,
     r and whether the criterion and the timings agree."""
