@@ -517,6 +517,13 @@ def run_fit(args):
     assert vl.last_error() == 0
     k, sh = cfg.top_k, cfg.n_shared
     model = X.fit_bandwidths(fit_w, k, eb, sh)
+    # the per-slot engine's re-read cost against a unique read (eq. (4)
+    # reading), over every window's per-slot times
+    rr = X.fit_reread_cost(fit_w + test_w, k, sh)
+    reread = {"c_u_us": round(1e6 * rr["c_u"], 3), "c_re_us": round(1e6 * rr["c_re"], 3),
+              "c_re_over_c_u": round(rr["ratio"], 3), "t0_us": round(1e6 * rr["t0"], 2),
+              "rms_us": round(1e6 * rr["rms"], 2), "points": rr["points"],
+              "unique_read_gbs": round(eb / rr["c_u"] / 1e9, 1)}
     ev = X.evaluate(model, test_w, k, eb, sh)
     ns = sorted(model)
     med = lambda xs: statistics.median(xs) if xs else float("nan")
@@ -544,7 +551,8 @@ def run_fit(args):
         "inside_bound_18": f"{sum(e['inside'] for e in ev)} of {len(ev)}",
         "sign_of_saving_predicted": f"{sum(e['sign_ok'] for e in ev)} of {len(ev)}",
         "criterion_19_certain_and_right": f"{agree} of {certain}",
-        "crossover_measured": cross_meas, "crossover_predicted": cross_pred}))
+        "crossover_measured": cross_meas, "crossover_predicted": cross_pred,
+        "reread_cost": reread}))
 
 
 def run_sweep_only(args):

@@ -124,6 +124,32 @@ def fit_bandwidths(windows: Iterable[Dict], k: int, expert_bytes: int, n_shared:
     return model
 
 
+def fit_reread_cost(windows: Iterable[Dict], k: int, n_shared: int = 0) -> Dict:
+    """The per-slot engine's cost of re-reading an expert against a unique
+    read (the page's c_re / c_u of its eq. (4), given only as a range per
+    engine in Table 1).  The page does not print eq. (4); the reading taken
+    here is the linear step time
+        t_slot = t0 + c_u * (U + shared) + c_re * (n*(k + shared) - U - shared):
+    each pass reads its union's experts once at c_u each, and every further
+    read of an expert another slot already named costs c_re.  Fitted by least
+    squares over windows (dicts with n, U, t_slot in seconds); returns t0,
+    c_u, c_re (seconds per expert read), their ratio and the fit's residual
+    RMS (seconds)."""
+    import numpy as np
+    rows = list(windows)
+    A, y = [], []
+    for w in rows:
+        unique = w["U"] + n_shared
+        reads = w["n"] * (k + n_shared)
+        A.append([1.0, float(unique), float(reads - unique)])
+        y.append(float(w["t_slot"]))
+    A, y = np.array(A), np.array(y)
+    coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+    t0, c_u, c_re = (float(c) for c in coef)
+    rms = float(np.sqrt(np.mean((A @ coef - y) ** 2)))
+    return dict(t0=t0, c_u=c_u, c_re=c_re, ratio=c_re / c_u, rms=rms, points=len(rows))
+
+
 def predict(model: Dict, n: int, U: int, k: int, expert_bytes: int, n_shared: int = 0) -> Dict:
     """Predicted time of each kernel (its memory term M = bytes / bandwidth)
     and predicted saving S = tau_slot - tau_dedup for one pass of n tokens with

@@ -109,3 +109,26 @@ def test_fit_predict_evaluate_recovers_a_known_model():
     ev = X.evaluate(model, wins, k, b, sh)
     assert all(e["inside"] and e["sign_ok"] for e in ev)
     assert all(abs(e["saving"] - e["saving_hat"]) < 1e-15 for e in ev)
+
+
+# ------------------------------------------- re-read cost (eq. (4) reading)
+def test_reread_fit_recovers_known_costs_and_the_no_cache_case():
+    rng = np.random.default_rng(3)
+    k, sh = 8, 1
+    t0, c_u, c_re = 4e-6, 6.3e-6, 2.1e-6
+    rows = []
+    for n in range(1, 13):
+        for _ in range(6):
+            U = int(rng.integers(k, min(256, n * k) + 1))
+            t = t0 + c_u * (U + sh) + c_re * (n * (k + sh) - U - sh)
+            rows.append(dict(n=n, U=U, t_slot=t))
+    f = X.fit_reread_cost(rows, k, sh)
+    assert abs(f["c_u"] - c_u) < 1e-12 and abs(f["c_re"] - c_re) < 1e-12
+    assert abs(f["t0"] - t0) < 1e-12 and abs(f["ratio"] - 1 / 3) < 1e-9 and f["rms"] < 1e-15
+    # a per-slot engine with no cache benefit: time grows with the reads alone,
+    # whether or not another slot named the expert -> c_re / c_u = 1
+    flat = [dict(n=r["n"], U=r["U"], t_slot=t0 + c_u * r["n"] * (k + sh)) for r in rows]
+    assert abs(X.fit_reread_cost(flat, k, sh)["ratio"] - 1) < 1e-9
+    # noise of 1% moves the ratio only a little
+    noisy = [dict(r, t_slot=r["t_slot"] * (1 + 0.01 * rng.standard_normal())) for r in rows]
+    assert abs(X.fit_reread_cost(noisy, k, sh)["ratio"] - 1 / 3) < 0.1
