@@ -141,8 +141,9 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     const void *act = h;  // bf16; the E4M3 kernel converts it to fp16 in registers
     // One 8-token MMA tile per pass over a work item: a segment with more
     // tokens (the shared expert has all n) takes several passes over its
-    // weights.  Wider tiles (2 or 4 per pass) run out of registers and
-    // reduction buffers and measure slower than the re-read costs.
+    // weights.  Wider tiles (2 or 4 per pass) fit in registers, but their
+    // activation rows leave the ring 3 or 4 stages, and they measured slower
+    // than the extra passes.
     const int n_tiles = 1;
     TcParams P;
     P.T = T;
