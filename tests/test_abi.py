@@ -186,3 +186,24 @@ def test_selection_calls_reject_bad_arguments_before_any_launch(lib):
                s0) == lib.MOE_ERR_INVALID_ARG
     assert eco(y, y, y, 1, 8, 1, 64, 4, 2, ctypes.c_double(1e-6), x, y, None, y, None,
                s0) == lib.MOE_ERR_ALIGNMENT
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    # a copy of the package with no libmoe_verify.so: importing the binding
+    # must raise, not fall back to anything on the CPU
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "moe_expert_ffn_gemv_gb300")
+    dst = tmp_path / "moe_expert_ffn_gemv_gb300"
+    shutil.copytree(src, dst, ignore=shutil.ignore_patterns("*.so", "__pycache__", "csrc"))
+    code = ("import sys; sys.path.insert(0, sys.argv[1])\n"
+            "try:\n"
+            "    import moe_expert_ffn_gemv_gb300.binding\n"
+            "except ImportError as e:\n"
+            "    print('IMPORT-ERROR', 'no CPU fallback' in str(e))\n"
+            "else:\n"
+            "    print('IMPORTED')\n")
+    r = subprocess.run([sys.executable, "-c", code, str(tmp_path)], capture_output=True, text=True,
+                       timeout=300)
+    assert r.stdout.strip() == "IMPORT-ERROR True", (r.stdout, r.stderr[-2000:])
