@@ -188,6 +188,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def clocks_rejected(clocks) -> bool:
+    """A timed region is rejected when its clock samples show a hardware or
+    thermal slowdown, or a median SM clock below 85% of the maximum with no
+    reason reported (power capping alone is kept)."""
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    reasons = set(clocks.get("reasons") or [])
+    if reasons & bad:
+        return True
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    return bool(sm and mx and sm < 0.85 * mx and not (reasons - {"unsampled"}))
+
+
 def traffic_from_profile():
     """DRAM bytes per dedup call from the committed ncu summary, if it was
     taken on the current kernel sources (else None)."""
@@ -259,24 +271,34 @@ def run_ours(args):
 
     # timed region: K passes back to back, then K expert calls back to back,
     # each bracketed by events on the launching stream
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            g_pass.replay()
-        t_end.record(stream)
-        d_start = torch.cuda.Event(enable_timing=True)
-        d_end = torch.cuda.Event(enable_timing=True)
-        d_start.record(stream)
-        for i in range(args.steps):
-            g_exp.replay()
-        d_end.record(stream)
+    def timed_region():
+        barrier(ws)
         torch.cuda.synchronize()
-    barrier(ws)
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws)
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for i in range(args.steps):
+                g_pass.replay()
+            t_end.record(stream)
+            d_start = torch.cuda.Event(enable_timing=True)
+            d_end = torch.cuda.Event(enable_timing=True)
+            d_start.record(stream)
+            for i in range(args.steps):
+                g_exp.replay()
+            d_end.record(stream)
+            torch.cuda.synchronize()
+        barrier(ws)
+        return t_start.elapsed_time(t_end), d_start.elapsed_time(d_end), clk.summary()
+
+    pass_ms, dedup_ms, clocks = timed_region()
+    # a region that saw a hardware or thermal slowdown, or SM clocks well below
+    # their maximum with no reason given (a clock lock), is measured once more;
+    # every rank takes the same decision
+    if max_over_ranks(1.0 if clocks_rejected(clocks) else 0.0, ws) > 0:
+        pass_ms, dedup_ms, clocks = timed_region()
+        clocks["remeasured"] = True
+    total_ms = max_over_ranks(pass_ms, ws)
     assert vl.last_error() == 0
     ms_per_step = total_ms / args.steps
     value = whole_job_gbs(union_bytes, ms_per_step, ws)
@@ -302,7 +324,7 @@ def run_ours(args):
     act_bytes = (n * CFG.d * 2 + 2 * slots * CFG.inter * 2 + 2 * slots * CFG.d * 4
                  + n * CFG.d * 2 + n * CFG.top_k * 4)
     alg_bytes = union_bytes + act_bytes
-    dedup_avg = d_start.elapsed_time(d_end) / args.steps
+    dedup_avg = dedup_ms / args.steps
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (dedup_avg * 1e-3) / 1e9
 
@@ -399,7 +421,7 @@ def run_ours(args):
                               "one step's copies overlap another step's pass "
                               "(two buffer pairs, a stream per copy direction)"},
             "gpu_launches": 2 * KERNELS_PER_PASS * args.steps - args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "cpu_baseline": cpu,
             "sweep": sweep,
         }
