@@ -71,6 +71,9 @@ def lib():
         L.orc_verify.restype = ctypes.c_int
         L.orc_verify.argtypes = [ctypes.POINTER(_Layer), p, p, ctypes.c_int, ctypes.c_int,
                                  p, p, p, p]
+        L.orc_verify_routed.restype = ctypes.c_int
+        L.orc_verify_routed.argtypes = [ctypes.POINTER(_Layer), p, p, ctypes.c_int, ctypes.c_int,
+                                        p, p, p, p]
         L.orc_topk_from_scores.argtypes = [p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, p, p]
         L.orc_union_plan.restype = ctypes.c_int
@@ -203,6 +206,32 @@ def verify(layer: Layer, h: np.ndarray, tokens=None, threads: int = 1):
     lib().orc_verify(ctypes.byref(c), _ptr(h), _ptr(tok), m, threads,
                      _ptr(ids), _ptr(w), _ptr(z), _ptr(y))
     return ids, w, z, y
+
+
+def verify_routed(layer: Layer, h: np.ndarray, ids: np.ndarray, tokens=None, threads: int = 1):
+    """verify() on a given routing: ids [m][k] int32 (row i the experts of
+    token tokens[i], all tokens if None; distinct ids in [0, N)) replace the
+    top-k.  Returns (w [m][k] f64, the gate of those ids on the fp64 scores;
+    z [m][N] f64; y [m][d] f64)."""
+    h = np.ascontiguousarray(h)
+    n = h.shape[0]
+    if tokens is None:
+        tok, m = None, n
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        assert tok.size == 0 or (tok.min() >= 0 and tok.max() < n)
+        m = tok.shape[0]
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    assert ids.shape == (m, layer.top_k)
+    assert ids.size == 0 or (ids.min() >= 0 and ids.max() < layer.n_experts)
+    assert all(len(set(r.tolist())) == layer.top_k for r in ids)
+    w = np.zeros((m, layer.top_k), dtype=np.float64)
+    z = np.zeros((m, layer.n_experts), dtype=np.float64)
+    y = np.zeros((m, layer.d), dtype=np.float64)
+    c = layer._c()
+    lib().orc_verify_routed(ctypes.byref(c), _ptr(h), _ptr(tok), m, threads, _ptr(ids),
+                            _ptr(w), _ptr(z), _ptr(y))
+    return w, z, y
 
 
 def topk_from_scores(scores: np.ndarray, k: int, mode: int):

@@ -259,6 +259,20 @@ static void route_token(const orc_layer *L, const void *hs, int t, int32_t *ids,
   free(h);
 }
 
+/* Router scores of token t and the gate of the given ids (a routing chosen
+ * elsewhere, e.g. a GPU's on fp32 scores that differ from the oracle's top-k
+ * only among scores closer than fp32 rounding): z = W_g h, w = gate(z, ids). */
+static void gate_given_token(const orc_layer *L, const void *hs, int t,
+                             const int32_t *ids, double *w, double *z) {
+  int d = L->d;
+  double *h = (double *)malloc(sizeof(double) * (size_t)d);
+  for (int c = 0; c < d; ++c)
+    h[c] = load_elem(hs, L->act_type, (size_t)t * d + c);
+  orc_router_scores(L, h, z);
+  orc_gate(z, L->n_experts, ids, L->top_k, L->gate, w);
+  free(h);
+}
+
 /* The layer output of token t from its routed ids and weights:
  * y = sum over j of w[j] * FFN_{ids[j]}(h), in slot order, then the shared
  * expert with weight 1.  With `keep` (NULL = every expert), a slot whose
@@ -286,7 +300,7 @@ static void ffn_token(const orc_layer *L, const void *hs, int t,
 }
 
 /* What a worker does for each of its tokens. */
-enum { DO_ROUTE_AND_FFN = 0, DO_ROUTE = 1, DO_FFN = 2 };
+enum { DO_ROUTE_AND_FFN = 0, DO_ROUTE = 1, DO_FFN = 2, DO_GATE_AND_FFN = 3 };
 
 typedef struct {
   const orc_layer *L;
@@ -308,7 +322,9 @@ static void *worker(void *p) {
     int t = A->tokens ? A->tokens[i] : i;
     int32_t *ids = A->ids + (size_t)i * L->top_k;
     double *w = A->w + (size_t)i * L->top_k;
-    if (A->mode != DO_FFN)
+    if (A->mode == DO_GATE_AND_FFN)
+      gate_given_token(L, A->hs, t, ids, w, A->z + (size_t)i * L->n_experts);
+    else if (A->mode != DO_FFN)
       route_token(L, A->hs, t, ids, w, A->z + (size_t)i * L->n_experts);
     if (A->mode != DO_ROUTE)
       ffn_token(L, A->hs, t, ids, w, A->keep, A->y + (size_t)i * L->d);
@@ -349,6 +365,18 @@ int orc_verify(const orc_layer *L, const void *hs, const int32_t *tokens,
                double *y) {
   run_workers(L, hs, tokens, n_tokens, n_threads, DO_ROUTE_AND_FFN, NULL, ids,
               w, z, y);
+  return 0;
+}
+
+/* orc_verify with the routing given: ids[i][0..k) are token tokens[i]'s
+ * experts (in [0, N), distinct), read instead of the top-k; the router
+ * scores, the gate of those ids and the layer output are computed as in
+ * orc_verify. */
+int orc_verify_routed(const orc_layer *L, const void *hs, const int32_t *tokens,
+                      int n_tokens, int n_threads, const int32_t *ids,
+                      double *w, double *z, double *y) {
+  run_workers(L, hs, tokens, n_tokens, n_threads, DO_GATE_AND_FFN, NULL,
+              (int32_t *)ids, w, z, y);
   return 0;
 }
 

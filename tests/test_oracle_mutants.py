@@ -59,6 +59,8 @@ MUTANTS = {
                             "const double score = P[v] / ((double)cost + 1.0);"),
     "ecospec_ties_to_higher_index": ("if (best < 0 || score > best_score) {",
                                      "if (best < 0 || score >= best_score) {"),
+    "given_routing_gated_on_top_k": ("  orc_router_scores(L, h, z);\n  orc_gate(z, L->n_experts, ids, L->top_k, L->gate, w);\n  free(h);\n}\n\n/* The layer output",
+                                     "  orc_router_scores(L, h, z);\n  orc_topk(z, L->n_experts, L->top_k, (int32_t *)ids);\n  orc_gate(z, L->n_experts, ids, L->top_k, L->gate, w);\n  free(h);\n}\n\n/* The layer output"),
     "budget_plan_not_stable": ("for (int p = 0; p < n_slots; ++p)\n      if (uniq[u] == ids[p])",
                                "for (int p = n_slots - 1; p >= 0; --p)\n      if (uniq[u] == ids[p])"),
 }

@@ -160,14 +160,14 @@ def test_router_scores_and_selection_closed_form():
     assert abs(y[0, 0] - expect) < 1e-14 and np.all(y[0, 1:] == 0)
 
 
-def _dense_numpy(wg, w13, w2, h, k, gate, sh=None):
+def _dense_numpy(wg, w13, w2, h, k, gate, sh=None, ids_given=None):
     """Every expert applied to every token with numpy matmuls, then the top-k
-    picked by numpy's lexsort and gated with scipy."""
+    picked by numpy's lexsort (or the given ids) and gated with scipy."""
     I = w13.shape[1] // 2
     z = h @ wg.T
     out = np.zeros((h.shape[0], w2.shape[1]))
     for t in range(h.shape[0]):
-        ids = np.lexsort((np.arange(z.shape[1]), -z[t]))[:k]
+        ids = np.lexsort((np.arange(z.shape[1]), -z[t]))[:k] if ids_given is None else ids_given[t]
         if gate == O.GATE_SOFTMAX:
             wts = scipy.special.softmax(z[t])[ids]
         elif gate == O.GATE_SOFTMAX_RENORM:
@@ -201,6 +201,29 @@ def test_layer_against_dense_numpy_formulation(gate, shared):
                        h.astype(np.float64), k, gate,
                        None if sh is None else tuple(s.astype(np.float64) for s in sh))
     np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("gate", [O.GATE_SOFTMAX, O.GATE_SOFTMAX_RENORM, O.GATE_SIGMOID_RENORM])
+@pytest.mark.parametrize("shared", [False, True])
+def test_given_routing_against_dense_numpy_formulation(gate, shared):
+    # verify_routed: any distinct ids in any order (here mostly not the top-k)
+    rng = np.random.default_rng(19 + gate + 3 * shared)
+    d, I, E, k, n = 24, 10, 7, 3, 6
+    f = lambda *s: rng.standard_normal(s).astype(np.float32)
+    wg, w13, w2, h = f(E, d), f(E, 2 * I, d) * 0.3, f(E, d, I) * 0.3, f(n, d)
+    sh = (f(2 * I, d) * 0.3, f(d, I) * 0.3) if shared else None
+    L = _f32_layer(d, I, E, k, gate, wg, w13, w2, sh)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(n)]).astype(np.int32)
+    w, z, y = O.verify_routed(L, h, ids.copy())  # the reference keeps its own copy of the routing
+    ref = _dense_numpy(wg.astype(np.float64), w13.astype(np.float64), w2.astype(np.float64),
+                       h.astype(np.float64), k, gate,
+                       None if sh is None else tuple(s.astype(np.float64) for s in sh),
+                       ids_given=ids)
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(z, h.astype(np.float64) @ wg.astype(np.float64).T, rtol=1e-12)
+    # a subset of tokens, threads: the same rows
+    w2_, z2, y2 = O.verify_routed(L, h, ids[[4, 1]].copy(), tokens=[4, 1], threads=2)
+    np.testing.assert_array_equal(y2, y[[4, 1]])
 
 
 def test_layer_is_linear_in_down_weights_and_invariant_to_expert_relabeling():
