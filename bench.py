@@ -6,13 +6,13 @@ block scales), n = 8 draft-tree tokens (BFS tree, 4 children under the root,
 2 below; child = 0.6 parent + 0.8 eps).  Synthetic, seeded weights and
 hidden states; weights resident in HBM.
 
-One step = one verification pass through the C ABI: router scores, top-k
-and union plan in one launch (moe_route_plan), then the deduplicating expert
-FFN and combine (moe_verify_dedup), recorded once into CUDA graphs and
-replayed.  `value` = union-expert bytes per pass
-(routed union + shared expert, weights and scales) / device time per pass.
-The expert bytes of one pass (~2.5 GB) exceed the 129 MB L2, so passes run
-back to back with no flush.
+One step = one verification pass through the C ABI (moe_verify_pass): router
+scores, top-k and union plan in one launch, then the deduplicating expert FFN
+(gate/up, down) and the combine, recorded once into a CUDA graph and
+replayed.  `value` = union-expert bytes per pass (routed union + shared
+expert, weights and scales) / device time per pass.  The expert bytes of one
+pass (1.76 GB at U = 39) exceed the 129 MB L2, so passes run back to back
+with no flush.
 
 Also printed: the expert kernels' roofline against the measured HBM copy
 bandwidth, the end-to-end number (hidden states copied from pinned host
@@ -43,9 +43,10 @@ CFG = synth.DSV3
 N_TOKENS = 8
 METRIC = "µs per MoE verify pass and union-byte HBM GB/s (% of GB300 peak) vs n tokens"
 WORKLOAD = "deepseek-v3-shaped fp8-e4m3 moe layer, n=8 draft-tree tokens (rho=0.6), dedup verify pass"
-NOMINAL_HBM_GBS = 7900.0
+NOMINAL_HBM_GBS = (7900.0, 8000.0)  # GB300 HBM3e nominal: 7.9 TB/s, "~8 TB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_PASS = 4  # route + top-k + plan (fused), gate/up, down, combine
+KERNELS_PER_PASS = 4  # route + top-k + plan (fused; E4M3: + fp16 rows), gate/up, down, combine
+KERNELS_PER_DEDUP_CALL = 4  # E4M3 fp16 rows, gate/up, down, combine
 
 
 def parse():
@@ -236,6 +237,15 @@ def make_workload(device="cuda"):
     return layer, h
 
 
+def bench_config(U, union_bytes, ws):
+    """The workload's config, the same on both arms."""
+    return {"workload": WORKLOAD, "n_tokens": N_TOKENS, "d": CFG.d, "experts": CFG.n_experts,
+            "top_k": CFG.top_k, "shared": CFG.n_shared, "inter": CFG.inter,
+            "U": U, "union_bytes_per_pass": union_bytes,
+            "l2": "inputs larger than L2 (union bytes per pass >> 129 MB), no flush",
+            "parallelism": f"replicas x{ws}"}
+
+
 def expert_bytes(mv, desc):
     wb, sb = mv.moe_expert_bytes(desc)
     return wb + sb
@@ -317,12 +327,12 @@ def run_ours(args):
                "iqr_us": [round(q(0.25), 2), round(q(0.75), 2)], "replays": args.steps}
 
     # algorithmic bytes of one moe_verify_dedup call: union expert bytes + the
-    # hidden states (bf16, read once), the intermediate a (fp16, written and
-    # read once per slot), the per-slot fp32 outputs (written, read), y (bf16)
-    # and the gate weights
+    # hidden states (bf16, read once), their fp16 rows (written and read
+    # once), the intermediate a (bf16, written and read once per slot), the
+    # per-slot fp32 outputs (written, read), y (bf16) and the gate weights
     slots = n * (CFG.top_k + CFG.n_shared)
-    act_bytes = (n * CFG.d * 2 + 2 * slots * CFG.inter * 2 + 2 * slots * CFG.d * 4
-                 + n * CFG.d * 2 + n * CFG.top_k * 4)
+    act_bytes = (n * CFG.d * 2 + 2 * n * CFG.d * 2 + 2 * slots * CFG.inter * 2
+                 + 2 * slots * CFG.d * 4 + n * CFG.d * 2 + n * CFG.top_k * 4)
     alg_bytes = union_bytes + act_bytes
     dedup_avg = dedup_ms / args.steps
     peak, peak_kind = measured_peaks()
@@ -378,13 +388,15 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / args.steps
     e2e_value = whole_job_gbs(union_bytes, e2e_ms, ws)
 
-    sweep = None
-    if not args.no_sweep and rank == 0:
-        sweep = engine_sweep(mv, layer, h_all, args.sweep_max, eb)
-
     cpu = None
+    oracle_ns = []
     if not args.no_cpu and rank == 0 and ws == 1:
         cpu = cpu_baseline(layer, h, union_bytes)
+        oracle_ns = [1, N_TOKENS, args.sweep_max]
+
+    sweep = None
+    if not args.no_sweep and rank == 0:
+        sweep = engine_sweep(mv, layer, h_all, args.sweep_max, eb, oracle_ns=oracle_ns)
 
     if rank == 0:
         out = {
@@ -400,15 +412,12 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "e4m3 weights x fp16 activations, fp32 accumulate",
             "data": "synthetic (seeded N(0,0.02^2) weights quantised per 128x128 block; tree hidden states)",
-            "config": {"workload": WORKLOAD, "n_tokens": n, "d": CFG.d, "experts": CFG.n_experts,
-                       "top_k": CFG.top_k, "shared": CFG.n_shared, "inter": CFG.inter,
-                       "U": U, "union_bytes_per_pass": union_bytes,
-                       "l2": "inputs larger than L2 (union bytes per pass >> 129 MB), no flush",
-                       "parallelism": f"replicas x{ws}"},
+            "config": bench_config(U, union_bytes, ws),
             "us_per_pass": round(1e3 * ms_per_step, 2),
             "us_per_pass_single_replays": replays,
             "us_dedup_call": round(1e3 * dedup_avg, 2),
-            "pct_of_nominal_8tbs_whole_pass": round(100 * value / ws / NOMINAL_HBM_GBS, 1),
+            "pct_of_nominal_whole_pass": {f"{g:.0f}_gbs": round(100 * value / ws / g, 1)
+                                          for g in NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_kind": peak_kind, "kernel": "moe_verify_dedup (gate/up + down + combine)",
@@ -420,7 +429,7 @@ def run_ours(args):
                     "copies": "every step copies its h in and its y out (pinned host); "
                               "one step's copies overlap another step's pass "
                               "(two buffer pairs, a stream per copy direction)"},
-            "gpu_launches": 2 * KERNELS_PER_PASS * args.steps - args.steps,
+            "gpu_launches": (KERNELS_PER_PASS + KERNELS_PER_DEDUP_CALL) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "sweep": sweep,
@@ -436,11 +445,13 @@ def flush_l2(buf_a, buf_b):
     buf_b.sum()               # ... then read more than L2, so no dirty lines remain
 
 
-def engine_sweep(mv, layer, h_all, n_max, eb, reps=5, n_min=1, cfg=None):
+def engine_sweep(mv, layer, h_all, n_max, eb, reps=5, n_min=1, cfg=None, oracle_ns=()):
     """µs per pass of each engine's expert call (after routing and planning,
     which are shared) for n = n_min..n_max, L2 flushed before each timed call;
     u_bar, r and the crossover as "Expert Bytes, Kernel Bandwidth and the Best
-    Draft Length" defines them (moe_expert_ffn_gemv_gb300/crossover.py)."""
+    Draft Length" defines them (moe_expert_ffn_gemv_gb300/crossover.py).
+    For each n in oracle_ns, the oracle's time for the same pass on the host
+    cores beside it (oracle_pass_times)."""
     from moe_expert_ffn_gemv_gb300 import crossover as X
     cfg = cfg or CFG
     vl = mv.VerifyLayer(layer, 64)
@@ -483,9 +494,20 @@ def engine_sweep(mv, layer, h_all, n_max, eb, reps=5, n_min=1, cfg=None):
              round(a_["beta_slot"] / 1e9, 1),
              None if reuse[a_["n"] - 1] is None else round(reuse[a_["n"] - 1], 3),
              round(X.uniform_reuse(a_["n"], cfg.top_k, cfg.n_experts), 3)] for a_ in an]
-    return {"columns": ["n", "U", "us_dedup", "us_perslot", "u_bar", "r", "gbs_dedup_union",
-                        "gbs_perslot_requested", "reuse_rho", "reuse_rho_uniform"],
+    cols = ["n", "U", "us_dedup", "us_perslot", "u_bar", "r", "gbs_dedup_union",
+            "gbs_perslot_requested", "reuse_rho", "reuse_rho_uniform"]
+    extra = {}
+    ns = sorted({m for m in oracle_ns if n_min <= m <= n_max})
+    if ns:
+        ot = oracle_pass_times(cfg, layer, h_all, ns)
+        cols += ["oracle_ms_all_cores", "oracle_ms_1_thread"]
+        for row in rows:
+            o = ot["per_n"].get(row[0])
+            row += [None, None] if o is None else [o["ms_all_cores"], o["ms_1_thread"]]
+        extra["oracle_host"] = ot["host"]
+    return {"columns": cols,
             "rows": rows,
+            **extra,
             "crossover_n": X.crossover([a_["n"] for a_ in an], [a_["t_dedup"] for a_ in an],
                                        [a_["t_slot"] for a_ in an]),
             "criterion_agrees": all(a_["criterion_dedup_faster"] == a_["measured_dedup_faster"]
@@ -585,7 +607,8 @@ def run_sweep_only(args):
     layer = synth.make_layer(cfg, seed=1, device="cuda")
     h_all = synth.make_hidden(cfg, 64, seed=3, device="cuda", rho=args.rho, sigma=args.sigma)
     eb = sum(mv.moe_expert_bytes(mv.make_desc(cfg, 64)))
-    sw = engine_sweep(mv, layer, h_all, args.sweep_max, eb, n_min=args.sweep_min, cfg=cfg)
+    sw = engine_sweep(mv, layer, h_all, args.sweep_max, eb, n_min=args.sweep_min, cfg=cfg,
+                      oracle_ns=[] if args.no_cpu else [1, 8, args.sweep_max])
     print(json.dumps({"sweep_config": cfg.name, "rho": args.rho if args.rho is not None else cfg.rho,
                       "sigma": args.sigma if args.sigma is not None else cfg.sigma,
                       "hidden": cfg.hidden, **sw}))
@@ -882,9 +905,34 @@ def run_stack(args):
 
 # ------------------------------------------------------------- cpu / oracle
 
-def oracle_inputs(layer, h):
+def host_info():
+    """The host's CPU model and core count (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"host_cores": os.cpu_count() or 1, "cpu_model": model or "unknown",
+            "machine": os.uname().machine}
+
+
+def oracle_inputs(layer, h, cfg=None):
     import numpy as np
     import oracle
+    cfg = cfg or CFG
     cpu = layer.to("cpu")
 
     def nb(t):
@@ -892,26 +940,75 @@ def oracle_inputs(layer, h):
             return None
         t = t.contiguous()
         return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
-    L = oracle.Layer(CFG.d, CFG.n_experts, CFG.top_k, CFG.inter, oracle.BF16, oracle.E4M3,
-                     oracle.GATE_SIGMOID_RENORM, nb(cpu.wg), nb(cpu.w13), nb(cpu.w2), nb(cpu.s13),
+    ot = {synth.F32: oracle.F32, synth.BF16: oracle.BF16, synth.E4M3: oracle.E4M3}
+    og = {synth.GATE_SOFTMAX: oracle.GATE_SOFTMAX,
+          synth.GATE_SOFTMAX_RENORM: oracle.GATE_SOFTMAX_RENORM,
+          synth.GATE_SIGMOID_RENORM: oracle.GATE_SIGMOID_RENORM}
+    L = oracle.Layer(cfg.d, cfg.n_experts, cfg.top_k, cfg.inter, ot[cfg.act], ot[cfg.wtype],
+                     og[cfg.gate], nb(cpu.wg), nb(cpu.w13), nb(cpu.w2), nb(cpu.s13),
                      nb(cpu.s2), nb(cpu.sh_w13), nb(cpu.sh_w2), nb(cpu.sh_s13), nb(cpu.sh_s2))
     return oracle, L, nb(h.cpu())
 
 
+def oracle_pass_times(cfg, layer, h_all, ns, reps=1):
+    """The oracle, as it stands, on the same seeded inputs: for each n, one
+    whole n-token pass with its tokens split over all host cores (the oracle
+    runs one token per thread, so it uses min(cores, n) threads), and the
+    single-thread time of a pass, taken as n x one token's single-thread time
+    (every token does the same work: all N router scores and k (+ shared)
+    SwiGLU experts)."""
+    oracle, L, hb = oracle_inputs(layer, h_all[:max(ns)].contiguous(), cfg)
+    cores = os.cpu_count() or 1
+    t1 = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.verify(L, hb, tokens=[0], threads=1)
+        t1.append(time.perf_counter() - t0)
+    tok = statistics.median(t1)
+    per_n = {}
+    for n in ns:
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            oracle.verify(L, hb, tokens=list(range(n)), threads=cores)
+            ts.append(time.perf_counter() - t0)
+        per_n[n] = {"ms_all_cores": round(1e3 * statistics.median(ts), 1),
+                    "threads": min(cores, n), "ms_1_thread": round(1e3 * n * tok, 1)}
+    return {"per_n": per_n,
+            "host": {**host_info(), "ms_1_thread_per_token": round(1e3 * tok, 1),
+                     "method": "all cores: the pass itself, tokens split over threads; "
+                               "1 thread: n x one token (median of 3)"}}
+
+
 def cpu_baseline(layer, h, union_bytes, reps=3):
-    """The oracle, as it stands, on all host cores: the whole n-token pass."""
+    """The oracle, as it stands, on the host cores: the whole n-token pass
+    with its tokens split over threads (min(cores, n) threads), and the
+    single-thread time of the same pass (n x one token's time)."""
     oracle, L, hb = oracle_inputs(layer, h)
     cores = os.cpu_count() or 1
+    threads = min(cores, N_TOKENS)
     ts = []
     for _ in range(reps):
         t0 = time.perf_counter()
         oracle.verify(L, hb, threads=cores)
         ts.append(time.perf_counter() - t0)
     t = statistics.median(ts)
-    return {"value": round(union_bytes / t / 1e9, 4), "unit": "GB/s", "cores": min(cores, N_TOKENS),
-            "kind": "oracle",
-            "sample": f"the whole {N_TOKENS}-token pass (fp64 per-token loop, tokens split over "
-                      f"threads), median of {reps}: {t:.2f} s per pass"}
+    t1 = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.verify(L, hb, tokens=[0], threads=1)
+        t1.append(time.perf_counter() - t0)
+    t_one = N_TOKENS * statistics.median(t1)
+    host = host_info()
+    return {"value": round(union_bytes / t / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", **host,
+            "sample": f"the whole {N_TOKENS}-token pass (fp64 per-token loop, one token per "
+                      f"thread: {threads} threads on {host['host_cores']} cores), median of "
+                      f"{reps}: {t:.2f} s per pass",
+            "single_thread": {"value": round(union_bytes / t_one / 1e9, 4), "unit": "GB/s",
+                              "s_per_pass": round(t_one, 2),
+                              "sample": f"one token on one thread, median of {reps}, x "
+                                        f"{N_TOKENS} tokens (each token does the same work)"}}
 
 
 # ---------------------------------------------------------------- reference
@@ -945,11 +1042,11 @@ def run_reference(args):
            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(1e3 * t, 1), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeds as ours)",
-           "config": {"workload": WORKLOAD, "n_tokens": N_TOKENS, "U": U,
-                      "union_bytes_per_pass": union_bytes},
+           "config": bench_config(U, union_bytes, ws),
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": min(cores, N_TOKENS),
-                            "kind": "oracle",
-                            "sample": f"the whole {N_TOKENS}-token pass per step on the host cores"},
+                            "kind": "oracle", **host_info(),
+                            "sample": f"the whole {N_TOKENS}-token pass per step, one token per "
+                                      f"thread ({min(cores, N_TOKENS)} threads)"},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out))

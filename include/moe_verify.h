@@ -269,8 +269,16 @@ moe_status moe_route_plan_budgeted(const moe_layer_desc *desc,
  *              of weight 0 is skipped in the sum)
  *   workspace  device, ws_bytes >= moe_workspace_bytes(desc)
  *   y          device [n][d] act_dtype (out)
- * The intermediate activations are kept in fp32 (F32 weights), bf16 (BF16
- * weights) or fp16 (E4M3 weights, whose values are exact in fp16).
+ * The intermediate activations a = silu(g) * u are kept in fp32 (F32
+ * weights) or bf16 (BF16 and E4M3 weights).  E4M3 weights are multiplied
+ * on fp16 tensor cores (every E4M3 value is exact in fp16): each token's
+ * hidden row, and each slot's row of a, reaches them scaled by the exact
+ * power of two that puts its largest magnitude in [2^14, 2^15), and the
+ * sums are scaled back in fp32.  So any finite bf16 hidden state is
+ * accepted, and within a row every element above 2^-28 of the row's
+ * largest keeps all its bits (smaller ones, whose terms cannot reach the
+ * output tolerance, lose bits or become 0).  Sums beyond fp32's range
+ * become inf, as in an fp32 accumulation.
  * The kernels check the plan before they use its indices: U outside [0, N],
  * a uniq entry outside [0, N), offs decreasing, negative or past n*k, or a
  * perm entry outside [0, n*k) makes moe_last_error() report
@@ -299,7 +307,9 @@ moe_status moe_verify_dedup(const moe_layer_desc *desc,
  *                                 otherwise not used and may be NULL)
  *   workspace  as moe_verify_dedup (its header also serves the routing)
  * The plan kernel hands the plan to the first expert kernel through a flag
- * in the workspace header, which the pass's last kernel clears; after a
+ * in the workspace header (with E4M3 weights it also writes the expert
+ * kernels' scaled fp16 rows of h, counted in a second header word), which
+ * the pass's last kernel clears; after a
  * call that failed (a non-OK status, or MOE_ERR_TIMEOUT from
  * moe_last_error), call moe_workspace_init before reusing the workspace.
  * n may be 0: the plan becomes empty and nothing else is enqueued. */
@@ -402,16 +412,22 @@ moe_status moe_workspace_init(void *workspace, size_t ws_bytes,
  * the library, held on every GPU that loads the library until the process
  * exits; the call itself allocates and frees nothing.
  *   - Limit: the scratch for n tokens must fit 16 MiB, i.e.
- *     256 + n*(k + n_shared)*(I*e + 4*d) bytes (each part rounded up to
- *     256 bytes; e = 4 for F32 weights, else 2); a larger call returns
- *     MOE_ERR_WORKSPACE and enqueues nothing (DeepSeek-V3 shapes: n <= 56).
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     256 + n*(k + n_shared)*(I*e + 4*d) bytes, plus for E4M3 weights
+ *     n*(2*d + 4) + 4*n*(k + n_shared) bytes (each part rounded up to 256
+ *     bytes; e = 4 for F32 weights, else 2); a larger call returns
+ *     MOE_ERR_WORKSPACE and enqueues nothing (DeepSeek-V3 shapes: n <= 54).
+ *   - Each call looks up the array's device address on the current device
+ *     (a stale address is never used, e.g. after a device reset).  A call
+ *     made while `stream` is being captured uses the address found by an
+ *     earlier call on that device; make that earlier call before any stream
+ *     capture (a first call during capture returns MOE_ERR_UNSUPPORTED).
  *   - Every call shares the array: calls whose execution may overlap on the
  *     GPU (other streams, other host threads) race; serialise them.
  *   - error_word: device int32 (4-byte aligned) that receives the call's
  *     device-side status (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_INPUT)
- *     once the call's work completes on `stream`; may be NULL. */
+ *     once the call's work completes on `stream`.  It may be NULL, but then
+ *     the device-side status is not reported anywhere, and on malformed
+ *     input (an id or plan the kernels reject) y is unspecified. */
 moe_status moe_verify_dedup_noalloc(const moe_layer_desc *desc,
                                     const moe_expert_weights *weights,
                                     const void *h, int32_t n,

@@ -92,10 +92,23 @@ moe_status check_weights(const moe_layer_desc &L, const moe_expert_weights *W) {
   return MOE_OK;
 }
 
+// Where the E4M3 engines' fp16 hidden rows live in a workspace.
+ActScaleOut act_scale_out(const moe_layer_desc &L, void *workspace, bool counted) {
+  const Workspace ws = workspace_layout(L);
+  uint8_t *wsb = static_cast<uint8_t *>(workspace);
+  ActScaleOut S;
+  S.h16 = reinterpret_cast<__half *>(wsb + ws.h16);
+  S.hshift = reinterpret_cast<int32_t *>(wsb + ws.hshift);
+  S.acts = counted ? reinterpret_cast<unsigned int *>(wsb + WS_ACTS_OFFSET) : nullptr;
+  return S;
+}
+
 // The expert FFN of one pass (both phases) and the combine, for either engine.
 // early_shared: the caller has just enqueued this pass's plan kernel on
 // `stream` (moe_verify_pass), so phase 1 may start the shared expert before
-// that kernel ends.
+// that kernel ends; that kernel has also written the E4M3 engines' fp16
+// hidden rows (counting them in the workspace header), which otherwise a
+// kernel of their own writes here.
 moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, const void *h, int n,
                        const int32_t *ids, const float *w, const moe_plan *plan, void *workspace,
                        void *y, cudaStream_t stream, bool early_shared = false) {
@@ -138,7 +151,12 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     if (e == cudaSuccess) e = launch_expert_f32(2, P, 2 * sms, stream);
   } else {
     const bool fp8 = L.w_dtype == MOE_E4M3_B128;
-    const void *act = h;  // bf16; the E4M3 kernel converts it to fp16 in registers
+    const void *act = h;  // bf16; E4M3: the fp16 rows of act_scale.cuh
+    const ActScaleOut S = act_scale_out(L, workspace, early_shared);
+    if (fp8) {
+      act = S.h16;
+      if (!early_shared) e = launch_act_scale(h, n, L.d, S, stream);
+    }
     // One 8-token MMA tile per pass over a work item: a segment with more
     // tokens (the shared expert has all n) takes several passes over its
     // weights.  Wider tiles (2 or 4 per pass) fit in registers, but their
@@ -151,6 +169,10 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.timeout_ns = timeout_ns(L);
     P.early_shared = early_shared && plan != nullptr;
     P.ready = P.early_shared ? ready : nullptr;
+    int32_t *ashift = reinterpret_cast<int32_t *>(wsb + ws.ashift);
+    P.hshift = S.hshift;
+    P.ashift = ashift;
+    P.acts = fp8 && P.early_shared ? S.acts : nullptr;
     P.inter = L.inter;
     const size_t es = w_size(L);
     // phase 1: gate/up over W13, K = d
@@ -163,6 +185,10 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.act = act;
     P.out = wsb + ws.inter;
     if (e == cudaSuccess) e = launch_expert_tc(fp8, 1, n_tiles, P, sms, stream);
+    // E4M3: each slot's row of a into fp16 range, in place
+    const int slots = n * (L.top_k + L.n_shared);
+    if (fp8 && e == cudaSuccess)
+      e = launch_a16_scale(wsb + ws.inter, slots, L.inter, ashift, sms, stream);
     // phase 2: down over W2, K = I
     P.w = static_cast<const uint8_t *>(W.w2);
     P.w_sh = static_cast<const uint8_t *>(W.sh_w2);
@@ -307,7 +333,9 @@ moe_status union_plan(const moe_layer_desc *desc, const int32_t *ids, const floa
 }
 
 // signal_ready: raise the plan-ready flag of the workspace once the plan is
-// written (moe_verify_pass only; its combine clears the flag).
+// written, and for E4M3 weights write the expert kernels' fp16 rows into the
+// workspace, counted in its header (moe_verify_pass only, whose workspace
+// has been checked whole; its combine clears both words).
 moe_status route_plan(const moe_layer_desc *desc, const void *router_w, const void *h, int32_t n,
                       int32_t budget, int32_t *ids, float *w, float *logits, const moe_plan *plan,
                       float *w_kept, int32_t *routed_u, void *workspace, size_t ws_bytes,
@@ -330,12 +358,14 @@ moe_status route_plan(const moe_layer_desc *desc, const void *router_w, const vo
   if (!aligned16(router_w) || !aligned16(h) || !aligned16(ids) || !aligned16(w) ||
       !aligned16(logits) || (w_kept && !aligned16(w_kept)))
     return MOE_ERR_ALIGNMENT;
+  ActScaleOut S = act_scale_out(*desc, workspace, true);
+  if (!signal_ready || desc->w_dtype != MOE_E4M3_B128) S.acts = nullptr;
   return cuda_status(launch_route_plan(
       desc->act_dtype == MOE_BF16, router_w, h, n, desc->d, desc->n_experts, desc->top_k,
       desc->gate, desc->n_shared, wb + sb, logits, ids, w, plan->hist, plan->uniq, plan->n_uniq,
       plan->offs, plan->perm, plan->union_bytes, budget, w_kept, routed_u, err,
       reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET),
-      signal_ready ? reinterpret_cast<unsigned int *>(wsb + WS_READY_OFFSET) : nullptr, st));
+      signal_ready ? reinterpret_cast<unsigned int *>(wsb + WS_READY_OFFSET) : nullptr, S, st));
 }
 
 }  // namespace
@@ -478,17 +508,25 @@ constexpr int NOALLOC_MAX_DEVICES = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_addr[NOALLOC_MAX_DEVICES] = {nullptr};
 
-// The array's device address on the current device, looked up once per
-// device (host code only holds a stand-in symbol, not a usable address).
-moe_status noalloc_scratch(void **out) {
+// The array's device address on the current device (host code only holds a
+// stand-in symbol, not a usable address).  Outside stream capture it is
+// looked up on every call, so that an address that changed (after a device
+// reset, the module is loaded again) is never used stale; during capture,
+// where the lookup may not run, the address found by an earlier call is
+// used, and without one the call returns MOE_ERR_UNSUPPORTED.
+moe_status noalloc_scratch(cudaStream_t st, void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES)
     return MOE_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_addr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
     g_noalloc_addr[dev] = p;
+  } else if (!g_noalloc_addr[dev]) {
+    return MOE_ERR_UNSUPPORTED;
   }
   *out = g_noalloc_addr[dev];
   return MOE_OK;
@@ -516,10 +554,10 @@ MOE_API moe_status moe_verify_dedup_noalloc(const moe_layer_desc *desc,
   moe_layer_desc L = *desc;
   L.n_max = n;
   if (workspace_layout(L).total > NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
-  void *scratch = nullptr;
-  s = noalloc_scratch(&scratch);
-  if (s != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void *scratch = nullptr;
+  s = noalloc_scratch(st, &scratch);
+  if (s != MOE_OK) return s;
   // the error word must start at zero; the rest is fully written before it is read
   if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
   s = run_experts(L, *weights, h, n, ids, w, plan, scratch, y, st);

@@ -27,11 +27,15 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const float *_
                                                                   int n, int k, int d,
                                                                   int n_shared,
                                                                   void *__restrict__ y,
-                                                                  uint32_t *ready) {
+                                                                  uint32_t *flags) {
   pdl_wait();  // the expert kernel's rows (launched as its programmatic dependent)
-  // Both expert kernels have ended, so no reader of the plan-ready flag is
-  // left: clear it for the next pass.
-  if (ready && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ready = 0u;
+  // Both expert kernels have ended, so no reader of moe_verify_pass's
+  // plan-ready flag and scaled-rows counter is left: clear them for the
+  // next pass.
+  if (flags && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    flags[0] = 0u;
+    flags[1] = 0u;
+  }
   const int t = blockIdx.y;
   const int c = (blockIdx.x * COMBINE_THREADS + threadIdx.x) * 4;
   if (c >= d) return;
@@ -80,13 +84,13 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const float *_
 }  // namespace
 
 cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,
-                           bool out_bf16, void *y, uint32_t *ready, cudaStream_t stream) {
+                           bool out_bf16, void *y, uint32_t *flags, cudaStream_t stream) {
   dim3 grid((d / 4 + COMBINE_THREADS - 1) / COMBINE_THREADS, n);
   if (out_bf16)
     return launch_dependent(combine_kernel<true>, grid, dim3(COMBINE_THREADS), 0, stream, yslot,
-                            w, n, k, d, n_shared, y, ready);
+                            w, n, k, d, n_shared, y, flags);
   return launch_dependent(combine_kernel<false>, grid, dim3(COMBINE_THREADS), 0, stream, yslot, w,
-                          n, k, d, n_shared, y, ready);
+                          n, k, d, n_shared, y, flags);
 }
 
 }  // namespace moe

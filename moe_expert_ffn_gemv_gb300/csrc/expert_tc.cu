@@ -10,7 +10,7 @@
 //                  are requested once per pair that names it.
 // and both halves of the SwiGLU FFN:
 //   PHASE 1  a = silu(W1 x) * (W3 x)  over gate rows [32 rb, 32 rb + 32) and the
-//            matching up rows, K = d; writes a[slot][I] (bf16 or fp16);
+//            matching up rows, K = d; writes a[slot][I] (bf16);
 //   PHASE 2  y_slot = W2 a           over rows [64 rb, 64 rb + 64) of W2, K = I;
 //            writes yslot[slot][d] (fp32).
 //
@@ -41,7 +41,12 @@
 //     banks;
 //   - E4M3 bytes become fp16 with cvt.rn.f16x2.e4m3x2 (exact); the block scale
 //     multiplies the fp32 partial sum of each 64-column chunk, which lies in a
-//     single 128x128 scale block;
+//     single 128x128 scale block.  The activations reach this fp16 MMA scaled
+//     into fp16 range by exact powers of two (act_scale.cuh): phase 1 streams
+//     the fp16 rows h16 = h * 2^hshift[t], its epilogue scales g and u back
+//     and stores a in bf16; a kernel between the phases rewrites each slot's
+//     row of a as fp16 times 2^ashift[slot], which phase 2 streams and its
+//     epilogue scales back;
 //   - after the last stage of an item each consumer warp drops its partial
 //     sums into a reduction buffer (two for BF16, one for E4M3, whose ring
 //     slots are larger) and goes on streaming; warp 9, the epilogue warp,
@@ -116,8 +121,11 @@ __device__ __forceinline__ float silu_times(float g, float u) {
 // The plan (or, per-slot, the routed ids) copied to shared memory at kernel
 // start, so that stepping from one work item to the next costs no global
 // round trip.
-constexpr int MAX_SLOTS = 64 * 32;
+constexpr int MAX_TOKENS = 64;
+constexpr int MAX_SLOTS = MAX_TOKENS * 32;
 constexpr int MAX_EXPERTS = 256;
+// every slot of a pass: n*k routed, then the shared expert's n*k + t
+constexpr int MAX_ALL_SLOTS = MAX_SLOTS + MAX_TOKENS;
 
 // Deduplicating segments: the shared expert first (segment 0, all n tokens;
 // it needs no plan), then the U routed experts in plan order.  Per-slot
@@ -240,8 +248,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   constexpr int ACT_ROW = act_row_bytes<FP8>();
   constexpr int ACT_OFF = act_offset<FP8>();  // a slot's activation rows
   constexpr int TRAILER = FP8 ? PACK_SCALE_BYTES : 0;  // scale bytes behind a tile
-  // E4M3 phase 1 reads the bf16 hidden states and converts them to fp16
-  constexpr bool BF16_ACT_TO_F16 = FP8 && PHASE == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t *ring = smem;
   float4 *red = reinterpret_cast<float4 *>(smem + S * SLOT);   // [RB][red_bytes]
@@ -256,6 +262,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   __shared__ int16_t s_tab[MAX_SLOTS];  // entries below 2048; -1 stands for any other
   __shared__ int32_t s_U;
   __shared__ uint64_t tables_bar;  // the plan is in shared memory (lazy phase 1)
+  // E4M3: phase 1's token shifts (hshift), phase 2's slot shifts (ashift),
+  // read by the epilogue warp
+  __shared__ int32_t s_hshift[FP8 && PHASE == 1 ? MAX_TOKENS : 1];
+  __shared__ int8_t s_ashift[FP8 && PHASE == 2 ? MAX_ALL_SLOTS : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = P.T.n * P.T.k;
@@ -278,6 +288,21 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   //    it copies phase 1's activations, which completes those stages.
   const bool lazy =
       PHASE == 1 && P.T.dedup && P.T.n_shared > 0 && P.early_shared && P.ready != nullptr;
+  // Lazy E4M3 phase 1 reads the fp16 rows that the plan kernel, still
+  // running, writes: the activation and epilogue warps wait (bounded) until
+  // it has counted every 8-token block, each lane acquiring the count itself.
+  const bool acts_flag = FP8 && PHASE == 1 && lazy && P.acts != nullptr;
+  auto await_acts = [&]() -> bool {
+    const uint32_t need = uint32_t((P.T.n + 7) / 8);
+    bool seen = true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(P.acts) < need)
+      if (globaltimer_ns() - t0 > P.timeout_ns) {
+        seen = false;
+        break;
+      }
+    return __all_sync(0xffffffffu, seen);
+  };
   // the plan (or, per-slot, the ids) into shared memory, threads first,
   // first + step, ... (the early-start mode has its own loader, below)
   auto load_tables = [&](int first, int step) {
@@ -366,6 +391,22 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     // (phase 2), and give the buffer back.
     bool aborted = false;
     uint32_t ep = 0;
+    if constexpr (FP8 && PHASE == 1) {
+      if (acts_flag && !await_acts()) {
+        aborted = true;
+        s_abort = 1;
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+      }
+      for (int i = lane; i < P.T.n; i += 32) s_hshift[i] = aborted ? 0 : __ldcg(P.hshift + i);
+      __syncwarp();
+    }
+    if constexpr (FP8 && PHASE == 2) {
+      // the kernel ahead rewrote a and wrote the slot shifts
+      pdl_wait();
+      const int n_all = nk + P.T.n_shared * P.T.n;
+      for (int i = lane; i < n_all; i += 32) s_ashift[i] = int8_t(__ldcg(P.ashift + i));
+      __syncwarp();
+    }
     Cursor cur;
     cursor_start(cur);
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
@@ -405,15 +446,22 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
             if (col >= m_left) continue;
             const int slot = T.slot(cur.sg, cur.grp * TOK + col);
             if (PHASE == 1) {
-              const float a = silu_times(vals[e], ups[e]);
+              float gv = vals[e], uv = ups[e];
+              if (FP8) {
+                // the rows were scaled by 2^hshift: scale the sums back
+                const float back = pow2f(-s_hshift[T.token(slot)]);
+                gv *= back;
+                uv *= back;
+              }
+              const float a = silu_times(gv, uv);
               uint16_t *out =
                   static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter + cur.rb * 32 + row;
-              if (FP8) *reinterpret_cast<__half *>(out) = __float2half_rn(a);
-              else *reinterpret_cast<__nv_bfloat16 *>(out) = __float2bfloat16_rn(a);
+              *reinterpret_cast<__nv_bfloat16 *>(out) = __float2bfloat16_rn(a);
             } else {
               float *out = static_cast<float *>(P.out) + int64_t(slot) * P.rows_total +
                            cur.rb * ROWS + row;
-              *out = vals[e];
+              // E4M3: a reached the MMA scaled by 2^ashift[slot]
+              *out = FP8 ? vals[e] * pow2f(-s_ashift[slot]) : vals[e];
             }
           }
         }
@@ -592,9 +640,14 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     const uint8_t *act = static_cast<const uint8_t *>(P.act);
     uint32_t it = 0;
     bool ok = true;
+    if (acts_flag) {
+      // lazy E4M3 phase 1: the fp16 rows come from the plan kernel
+      ok = await_acts();
+      fence_proxy_async_global();
+    }
     Cursor cur;
     cursor_start(cur);
-    bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
+    bool have = ok && cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
     while (have) {
       const int s = it % S;
       const uint32_t round = it / S;
@@ -679,18 +732,6 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
           bfr[nt][4 * v + 2] = x.z;
           bfr[nt][4 * v + 3] = x.w;
         }
-      }
-      if (BF16_ACT_TO_F16) {
-        // the hidden states arrive as bf16; the fp16 MMA wants fp16 pairs
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int v = 0; v < BW; ++v) {
-            const uint32_t x = bfr[nt][v];
-            const __half2 h2 =
-                __floats2half2_rn(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-            bfr[nt][v] = *reinterpret_cast<const uint32_t *>(&h2);
-          }
       }
       // the block scales of the warp's 64 columns (one 128-column block),
       // behind the tile: the gate rows' and the up rows' (phase 1), or the
@@ -801,7 +842,9 @@ cudaError_t launch_one(const TcParams &P, int grid, cudaStream_t stream) {
   auto kern = expert_tc_kernel<FP8, PHASE, NT>;
   constexpr size_t smem = smem_bytes<FP8, NT>();
   // 227 KB per CTA, of which the static plan tables take under 6.5 KB
-  static_assert(smem + 6656 <= 232448, "the ring does not fit in shared memory");
+  // (E4M3 phase 2 adds its 2.1 KB table of slot exponents)
+  static_assert(smem + 6656 + (FP8 && PHASE == 2 ? MAX_ALL_SLOTS : 0) <= 232448,
+                "the ring does not fit in shared memory");
   // the shared-memory opt-in is set once per device (the first call), so
   // later calls, e.g. under stream capture, only launch
   static unsigned long long configured = 0;

@@ -49,6 +49,14 @@ struct TcParams {
   // may then start the shared expert before that kernel ends
   int32_t early_shared;
   uint32_t *ready;  // early_shared: the plan kernel's plan-ready flag
+  // E4M3 weights (fp16 MMA; act_scale.cuh): phase 1's `act` is the fp16
+  // rows h16, token t scaled by 2^hshift[t], and it writes a in bf16; phase
+  // 2's `act` is a in fp16, row `slot` scaled by 2^ashift[slot].  Each phase
+  // scales its sums back.  With early_shared, the rows h16 come from the
+  // plan kernel, which counts the 8-token blocks it has written in *acts.
+  const int32_t *hshift;
+  const int32_t *ashift;
+  const uint32_t *acts;
 };
 
 // Tensor-core expert FFN (BF16 weights, or E4M3 with fp32 block scales);
@@ -77,6 +85,25 @@ cudaError_t launch_expert_f32(int phase, const F32Params &P, int grid, cudaStrea
 cudaError_t launch_pack(const void *src, const float *scales, void *dst, int n_matrices, int rows,
                         int kbytes, int inter, bool gate_up, cudaStream_t stream);
 
+// Where the E4M3 engines' fp16 hidden rows go (act_scale.cuh), in the workspace.
+struct ActScaleOut {
+  __half *h16;         // [n][d] fp16 rows, h[t] * 2^hshift[t]
+  int32_t *hshift;     // [n]
+  unsigned int *acts;  // launch_route_plan: blocks written so far (null: none)
+};
+
+// The E4M3 engines' fp16 rows of h [n][d] (bf16), one CTA per 8 tokens,
+// launched as a programmatic dependent of the kernel ahead (it waits for
+// that kernel before reading h).  (act_scale.cu)
+cudaError_t launch_act_scale(const void *h, int n, int d, const ActScaleOut &S,
+                             cudaStream_t stream);
+
+// The E4M3 engines' fp16 rows of a [slots][I]: each bf16 row rewritten in
+// place as fp16 times 2^ashift[slot], a warp per row, at most max_ctas CTAs;
+// launched as a programmatic dependent of the gate/up kernel.  (act_scale.cu)
+cudaError_t launch_a16_scale(void *a, int slots, int inter, int32_t *ashift, int max_ctas,
+                             cudaStream_t stream);
+
 // Router scores logits[t][e] = W_g[e] . h[t] (fp32 accumulation).
 cudaError_t launch_router_scores(bool bf16, const void *router_w, const void *h, int n, int d,
                                  int n_experts, float *logits, cudaStream_t stream);
@@ -89,12 +116,15 @@ cudaError_t launch_topk_gate(const float *logits, int n, int n_experts, int k, i
 // zeroed device word that the kernel leaves zeroed.  budget >= 0: the
 // budgeted plan (w_kept written, routed_u if not NULL); budget < 0: none.
 // `ready` (or null): set to 1 with release semantics once the plan is written.
+// S.acts (or null): bf16 activations only; the launch also writes the E4M3
+// engines' fp16 rows into S and counts each 8-token block in *S.acts (release).
 cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, int n, int d,
                               int n_experts, int k, int gate, int n_shared, int64_t expert_bytes,
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
                               int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-                              unsigned int *counter, unsigned int *ready, cudaStream_t stream);
+                              unsigned int *counter, unsigned int *ready, const ActScaleOut &S,
+                              cudaStream_t stream);
 
 // Expert union and slot permutation (one CTA).
 cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, int n_shared,
@@ -126,8 +156,9 @@ cudaError_t launch_ecospec_select(const int32_t *parent, const float *q, const i
                                   int32_t *err, cudaStream_t stream);
 
 // y[t] = sum_j w[t][j] yslot[t*k+j] (+ yslot[n*k+t]) -> y (fp32 or bf16).
-// `ready` (or null): the plan-ready flag of moe_verify_pass, cleared here.
+// `flags` (or null): moe_verify_pass's two header words, the plan-ready flag
+// and the scaled-rows counter, cleared here.
 cudaError_t launch_combine(const float *yslot, const float *w, int n, int k, int d, int n_shared,
-                           bool out_bf16, void *y, uint32_t *ready, cudaStream_t stream);
+                           bool out_bf16, void *y, uint32_t *flags, cudaStream_t stream);
 
 }  // namespace moe

@@ -66,6 +66,13 @@ __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Orders this thread's earlier generic-proxy view of global memory (e.g.
+// data another CTA published through a release / acquire pair) before its
+// later async-proxy accesses (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -203,16 +210,45 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_bytes, uint32_t 
       : "r"(four_bytes));
 }
 
+// --------------------------------------------------- fp16 range of E4M3 MMA
+//
+// The E4M3 engines multiply on fp16 tensor cores (every E4M3 value is an
+// fp16 value), so each activation row reaches them scaled by an exact power
+// of two 2^shift that puts its largest magnitude m in [2^14, 2^15): no
+// element overflows fp16, and every element above m * 2^-28 keeps all its
+// bf16 bits.  The sums are scaled back by 2^-shift in fp32.  `bits` are the
+// bits of m >= 0 as a float: shift = 14 - floor(log2 m), clamped to
+// [-113, 126] so that both 2^shift and 2^-shift are normal floats (a row
+// whose largest magnitude is below 2^-112 lands below 2^14, still exactly);
+// 0 for m = 0, inf or NaN (they pass through unchanged).
+__device__ __forceinline__ int fp16_range_shift(uint32_t bits) {
+  const int e = int(bits >> 23);  // biased exponent of m
+  if (bits == 0u || e >= 255) return 0;
+  const int s = 141 - e;          // 14 - (e - 127)
+  return s < -113 ? -113 : s > 126 ? 126 : s;
+}
+
+// 2^s as a float, for s in [-126, 127].
+__device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) << 23); }
+
 // --------------------------------------------------------------- workspace
 
 // Layout of the caller's workspace (all offsets 256-byte aligned):
 //   [0, 256)           header: int32 error word at byte 0, the fused
-//                      route + plan kernel's ticket counter at byte 64
+//                      route + plan kernel's ticket counter at byte 64,
+//                      moe_verify_pass's plan-ready flag at byte 72 and its
+//                      scaled-rows counter at byte 76
 //   inter              [n_max*(k+n_shared)][I] intermediate a = silu(g)*u
-//                      (fp32 for F32 weights, bf16 for BF16, fp16 for E4M3)
+//                      (fp32 for F32 weights, bf16 for BF16; E4M3: bf16 as
+//                      the gate/up kernel writes it, then fp16 in place, row
+//                      `slot` scaled by 2^ashift[slot])
 //   yslot              [n_max*(k+n_shared)][d] fp32 per-slot expert outputs
+//   E4M3 weights only:
+//   h16                [n_max][d] fp16: h[t] * 2^hshift[t]
+//   hshift             [n_max] int32
+//   ashift             [n_max*(k+n_shared)] int32
 struct Workspace {
-  size_t inter, yslot, total;
+  size_t inter, yslot, h16, hshift, ashift, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -221,16 +257,27 @@ constexpr size_t WS_TICKET_OFFSET = 64;
 // The plan-ready flag of moe_verify_pass: raised by its plan kernel once the
 // plan is written, read by its first expert kernel, cleared by its combine.
 constexpr size_t WS_READY_OFFSET = 72;
+// moe_verify_pass with E4M3 weights: the count of 8-token blocks whose
+// scaled rows (h16, hshift) its plan kernel has written; read by the first
+// expert kernel, cleared by the combine.
+constexpr size_t WS_ACTS_OFFSET = 76;
 
 inline Workspace workspace_layout(const moe_layer_desc &L) {
   const size_t slots = size_t(L.n_max) * size_t(L.top_k + L.n_shared);
   const size_t inter_es = L.w_dtype == MOE_F32 ? 4 : 2;
+  const bool e4m3 = L.w_dtype == MOE_E4M3_B128;
   Workspace w;
   size_t off = 256;
   w.inter = off;
   off += align256(slots * size_t(L.inter) * inter_es);
   w.yslot = off;
   off += align256(slots * size_t(L.d) * 4);
+  w.h16 = off;
+  off += e4m3 ? align256(size_t(L.n_max) * size_t(L.d) * 2) : 0;
+  w.hshift = off;
+  off += e4m3 ? align256(size_t(L.n_max) * 4) : 0;
+  w.ashift = off;
+  off += e4m3 ? align256(slots * 4) : 0;
   w.total = off;
   return w;
 }

@@ -11,9 +11,15 @@
 //                         run to run.
 //   topk_gate_kernel      one warp per token (topk_gate_warp, route_plan.cuh).
 //   route_plan_kernel     both of the above and the union plan in one launch
-//                         (the last CTA to finish its scores does the rest).
+//                         (the last CTA to finish its scores does the rest);
+//                         for moe_verify_pass with E4M3 weights, one more CTA
+//                         per 8 tokens writes their fp16 rows for the expert
+//                         kernels (act_scale.cuh).
 #include <math.h>
 
+#include <type_traits>
+
+#include "act_scale.cuh"
 #include "kernels.h"
 #include "moe_common.cuh"
 #include "route_plan.cuh"
@@ -125,22 +131,39 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict_
 // takes a ticket; the CTA that takes the last ticket (so all scores are
 // written) runs the top-k of every token (one warp per token) and then
 // union_plan_block (BUDGET: the budgeted plan), and resets the ticket
-// counter for the next call.
+// counter for the next call.  With `A.acts` set, the grid has one more CTA
+// column (blockIdx.x == n_experts): it writes the fp16 rows of its 8 tokens
+// (act_scale_block) and counts them in *A.acts with release semantics, for
+// the E4M3 expert kernel that starts before this kernel ends.  It takes no
+// ticket: the plan does not wait for it.
 template <typename T, bool BUDGET>
 __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
     const T *__restrict__ wg, const T *__restrict__ h, int n, int d, int n_experts, int k,
     int gate, int n_shared, int64_t expert_bytes, float *logits, int32_t *ids, float *w,
     int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
     int64_t *union_bytes, int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-    unsigned int *counter, unsigned int *ready) {
+    unsigned int *counter, unsigned int *ready, ActScaleOut A) {
   pdl_trigger();  // the expert kernel behind this one may launch (it waits for the plan)
-  router_scores_cta(wg, h, n, d, n_experts, logits);
+  if (blockIdx.x < unsigned(n_experts)) {
+    router_scores_cta(wg, h, n, d, n_experts, logits);
+  } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    const int t0 = blockIdx.y * TOKENS_PER_CTA;
+    act_scale_block(h, d, t0, min(TOKENS_PER_CTA, n - t0), A.h16, A.hshift);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // the rows are read by bulk copies (async proxy) of another kernel
+      fence_proxy_async_global();
+      __threadfence();
+      atomicAdd(A.acts, 1u);
+    }
+    return;
+  }
   __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // this CTA's scores before its ticket
     const unsigned int ticket = atomicAdd(counter, 1u);
-    s_last = ticket == gridDim.x * gridDim.y - 1;
+    s_last = ticket == unsigned(n_experts) * gridDim.y - 1;  // the router CTAs
   }
   __syncthreads();
   if (!s_last) return;
@@ -201,16 +224,21 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
                               int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-                              unsigned int *counter, unsigned int *ready, cudaStream_t stream) {
-  dim3 grid(n_experts, (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
+                              unsigned int *counter, unsigned int *ready, const ActScaleOut &S,
+                              cudaStream_t stream) {
+  // E4M3 rows are written only beside bf16 activations (the only kind E4M3 weights take)
+  const bool scale = S.acts != nullptr && bf16;
+  dim3 grid(n_experts + (scale ? 1 : 0), (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
   const int threads = router_warps(d) * 32;
   const __nv_bfloat16 *wb = static_cast<const __nv_bfloat16 *>(router_w);
   const __nv_bfloat16 *hb = static_cast<const __nv_bfloat16 *>(h);
   const float *wf = static_cast<const float *>(router_w);
   const float *hf = static_cast<const float *>(h);
+  ActScaleOut Sx = S;
+  if (!scale) Sx.acts = nullptr;
 #define MOE_ROUTE_PLAN_ARGS                                                                  \
   n, d, n_experts, k, gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, \
-      perm, union_bytes, budget, w_kept, routed_u, err, counter, ready
+      perm, union_bytes, budget, w_kept, routed_u, err, counter, ready, Sx
   if (budget < 0) {
     if (bf16)
       route_plan_kernel<__nv_bfloat16, false><<<grid, threads, 0, stream>>>(wb, hb,

@@ -8,6 +8,8 @@ oracle can both be fed from it without sharing any code of the method.
 Distributions (readings of the workload descriptions, stated once here):
   expert weights  N(0, 0.02^2);  router weights N(0, 1/d);
   chain           h_0 ~ N(0, I), h_t = rho h_{t-1} + sqrt(1 - rho^2) eps_t;
+  wide range      unit normal elements multiplied by 1e5 or 1e-6 (a test of
+                  the fp16 range handling; see make_hidden);
   tree            BFS-numbered, node 0 the root, 4 children under the root
                   and 2 under every deeper node; child = parent + sigma eps
                   ("parent + N(0, sigma^2)") or, for the FP8 layer,
@@ -192,6 +194,17 @@ def make_hidden(cfg: LayerConfig, n: int, seed: int = 3, device="cpu", kind: Opt
             h[t] = rho * h[par[t]] + c * eps[t]
     elif kind == "identical":
         h[:] = eps[0]
+    elif kind == "wide_range":
+        # magnitudes far outside fp16's range, for the E4M3 engines' scaling:
+        # token 0 all x1e5, token 1 all x1e-6, the others a mix per element
+        # (2% x1e5, 40% x1e-6, the rest unit normal)
+        h[:] = eps[:max(n, 1)]
+        u = torch.rand(max(n, 1), cfg.d, generator=g, device=device, dtype=torch.float64)
+        mul = torch.where(u < 0.02, 1e5, torch.where(u < 0.42, 1e-6, 1.0))
+        mul[0] = 1e5
+        if n > 1:
+            mul[1] = 1e-6
+        h *= mul
     else:
         raise ValueError(kind)
     return h[:n].to(torch_dtype(cfg.act)).contiguous()

@@ -55,6 +55,29 @@ def rel_err(y, y_ref) -> float:
     return float(np.max(np.abs(y - y_ref) / den))
 
 
+def router_delta(layer: synth.Layer, h: torch.Tensor) -> np.ndarray:
+    """Per token: delta = 1e-5 * max_e sum_i |Wg[e][i] h[i]|, a bound on the
+    error of an fp32 accumulation of its router dot products (see tie_margin)."""
+    wg = np.asarray(layer.wg.float().cpu().numpy(), dtype=np.float64)
+    hh = np.asarray(h.float().cpu().numpy(), dtype=np.float64)
+    return 1e-5 * (np.abs(hh) @ np.abs(wg).T).max(axis=1)
+
+
+def topk_within(z_row: np.ndarray, ids: np.ndarray, k: int, tol: float) -> bool:
+    """ids (k distinct experts, in the order a GPU emitted them) are a top-k
+    of the exact scores z_row up to score errors of tol: every selected
+    score is at least the exact k-th largest minus tol, every other score at
+    most the k-th largest plus tol, and the order descends up to tol."""
+    ids = np.asarray(ids)
+    if len(set(ids.tolist())) != k:
+        return False
+    zk = np.sort(z_row)[::-1][k - 1]
+    sel = np.zeros(z_row.shape[0], dtype=bool)
+    sel[ids] = True
+    return bool(np.all(z_row[sel] >= zk - tol) and np.all(z_row[~sel] <= zk + tol)
+                and np.all(z_row[ids[:-1]] >= z_row[ids[1:]] - tol))
+
+
 def tie_margin(layer: synth.Layer, h: torch.Tensor, z: np.ndarray, k: int) -> np.ndarray:
     """Per token: the smallest gap between consecutive oracle scores among the
     first k+1 (in sorted order), over delta = 1e-5 * max_e sum_i |Wg[e][i] h[i]|,
@@ -62,10 +85,7 @@ def tie_margin(layer: synth.Layer, h: torch.Tensor, z: np.ndarray, k: int) -> np
     (it exceeds (terms per accumulator + tree depth) * 2^-24 * sum |.| by
     several times at d <= 8192).  A token with margin > 1 must be routed
     exactly as the oracle routes it."""
-    wg = np.asarray(layer.wg.float().cpu().numpy(), dtype=np.float64)
-    hh = np.asarray(h.float().cpu().numpy(), dtype=np.float64)
-    absdot = np.abs(hh) @ np.abs(wg).T                     # [n][E]
-    delta = 1e-5 * absdot.max(axis=1)
+    delta = router_delta(layer, h)
     out = np.empty(z.shape[0])
     for t in range(z.shape[0]):
         s = np.sort(z[t])[::-1][:k + 1]

@@ -3,7 +3,8 @@
 The GPU engines get the oracle's own routing (ids, and gate weights rounded
 to fp32) so that these tests isolate the expert arithmetic; routing has its
 own tests.  Sizes span several stages of the weight pipeline, ragged K
-tails, 1, 2 and 4 token tiles and segments larger than one pass of tiles.
+tails, and segments of more than 8 tokens (the width of one MMA token tile,
+so such a segment takes several passes over its weights).
 """
 import numpy as np
 import pytest
