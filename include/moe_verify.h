@@ -60,7 +60,7 @@
  *   - Limits (else MOE_ERR_UNSUPPORTED): N <= 256, 1 <= k <= min(N, 32),
  *     0 <= n <= n_max <= 64, n_shared 0 or 1, d % 8 == 0; F32 weights go with
  *     F32 activations and need I % 4 == 0; BF16 and E4M3 weights go with BF16
- *     activations; BF16 needs d % 64 == 0 and I % 32 == 0, E4M3 needs
+ *     activations; BF16 needs d % 64 == 0 and I % 64 == 0, E4M3 needs
  *     d % 128 == 0, I % 128 == 0, d <= 8192 and I <= 8192.
  */
 #ifndef MOE_VERIFY_H
@@ -157,9 +157,14 @@ moe_status moe_packed_bytes(const moe_layer_desc *desc, int64_t *w13_bytes,
  * E4M3: each expert matrix becomes a sequence of tiles of 64 rows x 512
  * bytes (the last tile of a row block narrower when a row is not a multiple
  * of 512 bytes); a W13 tile holds gate rows 32b..32b+31 followed by up rows
- * I+32b..I+32b+31; inside a tile the 16-byte pieces are ordered [64-byte
- * column chunk][16-row tile][row half][lane] so that one pipeline stage is
- * one contiguous bulk copy.  E4M3: every tile is followed by its 8 block
+ * I+32b..I+32b+31; tiles of a row block follow each other in K order, row
+ * blocks follow each other, so that one pipeline stage is one contiguous
+ * bulk copy.  Inside a tile, BF16: [128-byte column q][8-row group m][row r]
+ * [16-byte chunk], where chunk j of row 8m+r (bytes 128q+16j..+15 of K) is
+ * stored at position j XOR r (the tensor cores' 128-byte swizzled K-major
+ * layout); E4M3: the 16-byte pieces are ordered [64-byte column chunk]
+ * [16-row tile][row half][lane] (lane = 4 g + c takes row 16 t + 8 h + g,
+ * bytes 64 w + 16 c of the chunk).  E4M3: every tile is followed by its 8 block
  * scales from s13 / s2 (device, [n_matrices][rows/128][cols/128] float as in
  * the layout above; NULL for other weight types): the scales of the tile's
  * four 128-column blocks for the 128-row block of its first 32 rows, then

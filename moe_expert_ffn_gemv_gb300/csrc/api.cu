@@ -45,7 +45,8 @@ moe_status check_desc(const moe_layer_desc *L) {
       if (L->inter % 4) return MOE_ERR_UNSUPPORTED;
       break;
     case MOE_BF16:
-      if (L->d % 64 || L->inter % 32) return MOE_ERR_UNSUPPORTED;
+      // whole 128-byte columns of the swizzled tile layout in W13 and W2
+      if (L->d % 64 || L->inter % 64) return MOE_ERR_UNSUPPORTED;
       break;
     default:
       if (L->d % 128 || L->inter % 128) return MOE_ERR_UNSUPPORTED;

@@ -29,16 +29,19 @@
 //     stages late, and stalls it.  A warp's issue time per copy is what
 //     keeps it from running further ahead, hence one copy a stage for the
 //     weight stream (no separate scale copy; the rows on their own warp);
-//   - warps 0..7 consume: warp w owns bytes [64 w, 64 w + 64) of every row of a
-//     stage, i.e. a K-split across warps, and runs mma.sync m16n8k16 with the
-//     weights as the 16-row A operand (4 row tiles) and the segment's tokens as
-//     the 8-wide N operand (NT tiles).  Because a dot product does not depend
-//     on the order of its terms, each thread's 16 contiguous weight bytes feed
+//   - warps 0..7 consume: warp w owns 64 bytes of every row of a stage (a
+//     K-split across warps) and runs mma.sync m16n8k16 with the weights as
+//     the 16-row A operand (4 row tiles) and the segment's tokens as the
+//     8-wide N operand (NT tiles).  Because a dot product does not depend on
+//     the order of its terms, each thread's 16 contiguous weight bytes feed
 //     the A fragment directly (no ldmatrix); the activations (B fragment) are
-//     read with the same permutation of K.  Each warp reads its 4 KB of a
-//     stage with lane-contiguous 16-byte loads (no bank conflicts), and its
-//     tokens' activations from rows padded apart so that they hit distinct
-//     banks;
+//     read with the same permutation of K.  E4M3: warp w owns bytes
+//     [64 w, 64 w + 64), the tile's pieces are in the threads' order (lane-
+//     contiguous 16-byte loads).  BF16 (tiles in the 128-byte swizzled layout
+//     that tcgen05 also reads, pack.cu): warp w owns the chunks j = 2 c +
+//     w % 2 (thread c) of the 128-byte column w / 2, so a wavefront of 8 lanes
+//     (rows g, g + 1) covers 8 distinct bank groups.  The tokens' activation
+//     rows are padded apart so that they hit distinct banks;
 //   - E4M3 bytes become fp16 with cvt.rn.f16x2.e4m3x2 (exact); the block scale
 //     multiplies the fp32 partial sum of each 64-column chunk, which lies in a
 //     single 128x128 scale block.  The activations reach this fp16 MMA scaled
@@ -90,10 +93,12 @@ template <int NT>
 constexpr size_t red_bytes() { return size_t(CONSUMERS) * 4 * NT * 32 * 16; }
 
 // One activation row of a stage: its K columns as 16-bit values, plus a pad
-// that puts consecutive rows 4 (E4M3) or 16 (BF16) banks apart, so that the
-// consumers' 16-byte reads of two tokens' rows never meet in a bank.
+// of 16 bytes (4 banks) that sets consecutive rows apart, so that the
+// consumers' 16-byte reads of two tokens' rows never meet in a bank (BF16:
+// the chunks a warp reads in a row all have the parity of w % 2, and the pad
+// flips it from one token to the next).
 template <bool FP8>
-constexpr int act_row_bytes() { return KBYTES / (FP8 ? 1 : 2) * 2 + (FP8 ? 16 : 64); }
+constexpr int act_row_bytes() { return KBYTES / (FP8 ? 1 : 2) * 2 + 16; }
 
 // where a slot's activation rows start: behind the largest tile
 template <bool FP8>
@@ -708,7 +713,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     const int s = it % S;
     const uint32_t round = it / S;
     const int m_left = cur.sg.m - cur.grp * TOK;
-    const bool active = cur.ks * KBYTES + warp * 64 < kbytes;
+    // (a BF16 K tail is whole 128-byte columns, an E4M3 one whole 64-byte chunks)
+    const bool active = cur.ks * KBYTES + (FP8 ? warp * 64 : (warp >> 1) * 128) < kbytes;
     if (!aborted && s_abort) aborted = true;
     if (!aborted && !mbar_wait_bounded(&full[s], round & 1, P.timeout_ns)) {
       aborted = true;
@@ -722,8 +728,10 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       uint32_t bfr[NT][BW];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
+        // the K elements of this thread's weight bytes
+        const int k_el = FP8 ? warp * 64 + 16 * c : (warp >> 1) * 64 + 8 * (2 * c + (warp & 1));
         const uint4 *src = reinterpret_cast<const uint4 *>(
-            slot + ACT_OFF + (nt * 8 + g) * ACT_ROW + (warp * 64 / ES + (FP8 ? 16 * c : 8 * c)) * 2);
+            slot + ACT_OFF + (nt * 8 + g) * ACT_ROW + k_el * 2);
 #pragma unroll
         for (int v = 0; v < BW / 4; ++v) {
           const uint4 x = src[v];
@@ -746,12 +754,17 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       // this warp's 4 KB of the stage: [row tile mt][half h][lane][16 bytes];
       // all of it first, then the MMAs with the four row tiles' chains
       // interleaved (consecutive MMAs are independent)
-      const uint4 *st = reinterpret_cast<const uint4 *>(slot) + warp * 256 + lane;
+      // E4M3: [warp][row tile][half][lane]; BF16: row 8 m + g (m = 2 mt + half)
+      // of column w / 2 at chunk position (2 c + w % 2) ^ g, groups 64 pieces apart
+      const uint4 *st =
+          reinterpret_cast<const uint4 *>(slot) +
+          (FP8 ? warp * 256 + lane : (warp >> 1) * 512 + g * 8 + ((2 * c + (warp & 1)) ^ g));
+      constexpr int GROUP = FP8 ? 32 : 64;  // pieces between consecutive row halves
       uint32_t wl[4][4], wh[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
-        const uint4 lo = st[(mt * 2 + 0) * 32];
-        const uint4 hi = st[(mt * 2 + 1) * 32];
+        const uint4 lo = st[(mt * 2 + 0) * GROUP];
+        const uint4 hi = st[(mt * 2 + 1) * GROUP];
         wl[mt][0] = lo.x; wl[mt][1] = lo.y; wl[mt][2] = lo.z; wl[mt][3] = lo.w;
         wh[mt][0] = hi.x; wh[mt][1] = hi.y; wh[mt][2] = hi.z; wh[mt][3] = hi.w;
       }

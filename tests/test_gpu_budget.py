@@ -128,7 +128,7 @@ FUSED_CASES = [(synth.TINY, 4, 3), (synth.OLMOE, 8, 20), (synth.QWEN3, 61, 40),
 
 @pytest.mark.parametrize("cfg,n,B", FUSED_CASES, ids=lambda x: getattr(x, "name", str(x)))
 def test_fused_budgeted_route_plan_equals_separate_calls(mv, cfg, n, B):
-    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 32)
+    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 64)
     layer = synth.make_layer(small, seed=31).to("cuda")
     vl = mv.VerifyLayer(layer, 64)
     k = small.top_k
@@ -193,7 +193,7 @@ PASS_CASES = [
     (synth.shrink(synth.DSV3, 1024, 256, 32, "dsv3-small"), 8),
     (synth.shrink(synth.DSV3, 1024, 256, 32, "dsv3-small"), 33),
     (synth.shrink(synth.OLMOE, 512, 128), 16),
-    (synth.shrink(synth.QWEN3, 512, 96), 61),
+    (synth.shrink(synth.QWEN3, 512, 192), 61),
     (synth.TINY, 4),
 ]
 

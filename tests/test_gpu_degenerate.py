@@ -24,7 +24,7 @@ CASES = [
                       hidden="chain", rho=0.5),
     synth.LayerConfig("fp8-one-expert-shared", 256, 1, 1, 128, synth.BF16, synth.E4M3,
                       synth.GATE_SIGMOID_RENORM, n_shared=1, hidden="tree_ar", rho=0.6),
-    synth.LayerConfig("bf16-k-equals-n", 192, 4, 4, 96, synth.BF16, synth.BF16,
+    synth.LayerConfig("bf16-k-equals-n", 192, 4, 4, 128, synth.BF16, synth.BF16,
                       synth.GATE_SOFTMAX_RENORM, hidden="chain", rho=0.0),
     synth.LayerConfig("fp8-k-equals-n-shared", 256, 3, 3, 128, synth.BF16, synth.E4M3,
                       synth.GATE_SIGMOID_RENORM, n_shared=1, hidden="tree_ar", rho=0.6),

@@ -66,7 +66,7 @@ def check_layer(mv, cfg, n, seed=1, kind=None, rho=None, sigma=None, engines=("d
     return out, ids
 
 
-BF16_SMALL = synth.shrink(synth.OLMOE, d=704, inter=96, n_experts=12, name="bf16-d704-i96")
+BF16_SMALL = synth.shrink(synth.OLMOE, d=704, inter=192, n_experts=12, name="bf16-d704-i192")
 BF16_SMALL = synth.LayerConfig(**{**BF16_SMALL.__dict__, "top_k": 3})
 FP8_SMALL = synth.shrink(synth.DSV3, d=640, inter=384, n_experts=10, name="fp8-d640-i384")
 FP8_SMALL = synth.LayerConfig(**{**FP8_SMALL.__dict__, "top_k": 4})

@@ -1,6 +1,7 @@
 """moe_pack_expert_weights writes the tile layout include/moe_verify.h states
-(E4M3: each tile followed by its 8 block scales), checked piece by piece
-against a numpy transcription of that statement."""
+(BF16: 128-byte swizzled K-major columns; E4M3: fragment-ordered pieces, each
+tile followed by its 8 block scales), checked piece by piece against a numpy
+transcription of that statement."""
 import numpy as np
 import pytest
 import torch
@@ -23,9 +24,25 @@ def expected_packed(mat: np.ndarray, gate_up: bool, inter: int, scales=None) -> 
     tiles = (rows // 64) * ((K + 511) // 512)
     out = np.empty(rows * K + (32 * tiles if scales is not None else 0), dtype=np.uint8)
     pos = 0
+    def row_of(rit, rb):
+        if gate_up:
+            return 32 * rb + rit if rit < 32 else inter + 32 * rb + rit - 32
+        return 64 * rb + rit
+
     for rb in range(rows // 64):
         for kc in range((K + 511) // 512):
             width = min(512, K - 512 * kc)
+            if scales is None:
+                # BF16: [128-byte column q][8-row group m][row r][position], chunk j
+                # of row 8m+r at position j XOR r
+                for q in range(width // 128):
+                    for m in range(8):
+                        for r in range(8):
+                            for p in range(8):
+                                col = 512 * kc + 128 * q + 16 * (p ^ r)
+                                out[pos:pos + 16] = mat[row_of(8 * m + r, rb), col:col + 16]
+                                pos += 16
+                continue
             for w in range(width // 64):
                 for mt in range(4):
                     for h in range(2):
@@ -54,8 +71,8 @@ def expected_packed(mat: np.ndarray, gate_up: bool, inter: int, scales=None) -> 
     return out
 
 
-@pytest.mark.parametrize("wtype,d,inter", [(synth.BF16, 704, 96), (synth.E4M3, 640, 384),
-                                           (synth.BF16, 2880, 96)])
+@pytest.mark.parametrize("wtype,d,inter", [(synth.BF16, 704, 192), (synth.E4M3, 640, 384),
+                                           (synth.BF16, 2880, 192)])
 def test_pack_layout(mv, wtype, d, inter):
     cfg = synth.LayerConfig("pack", d, 3, 2, inter, synth.BF16, wtype, synth.GATE_SOFTMAX)
     layer = synth.make_layer(cfg, seed=9, device="cuda")

@@ -112,7 +112,7 @@ ROUTE_PLAN_CASES = [(synth.TINY, 4), (synth.OLMOE, 8), (synth.QWEN3, 61), (synth
 def test_fused_route_plan_equals_separate_calls(mv, cfg, n):
     # one launch (scores, top-k, gate, plan) == moe_route_topk then moe_union_plan, bit for bit,
     # on three calls in a row (the ticket counter must reset itself)
-    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 32)
+    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 64)
     layer = synth.make_layer(small, seed=31).to("cuda")
     vl = mv.VerifyLayer(layer, 64)
     for rep in range(3):
@@ -142,7 +142,7 @@ def test_fused_route_plan_equals_separate_calls(mv, cfg, n):
 
 
 def test_fused_route_plan_empty(mv):
-    layer = synth.make_layer(synth.shrink(synth.OLMOE, 2048, 32), seed=3).to("cuda")
+    layer = synth.make_layer(synth.shrink(synth.OLMOE, 2048, 64), seed=3).to("cuda")
     vl = mv.VerifyLayer(layer, 8)
     vl.plan.n_uniq.fill_(5)
     vl.route_plan(torch.empty(0, 2048, dtype=torch.bfloat16, device="cuda"), 0)

@@ -64,7 +64,7 @@ ROUTE_CASES = [
 @pytest.mark.parametrize("cfg,n", ROUTE_CASES, ids=lambda x: getattr(x, "name", str(x)))
 def test_route_from_hidden_states(mv, cfg, n):
     # only the router matters here: a layer with tiny experts and the real router
-    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 32)
+    small = synth.shrink(cfg, cfg.d, 128 if cfg.wtype == synth.E4M3 else 64)
     layer = synth.make_layer(small, seed=11)
     h = synth.make_hidden(small, n, seed=13)
     desc = mv.make_desc(small, n)

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     synth.LayerConfig("fp8-noalloc", 640, 10, 4, 384, synth.BF16, synth.E4M3,
                       synth.GATE_SIGMOID_RENORM, n_shared=1, hidden="tree_ar", rho=0.6),
-    synth.LayerConfig("bf16-noalloc", 704, 12, 3, 96, synth.BF16, synth.BF16,
+    synth.LayerConfig("bf16-noalloc", 704, 12, 3, 192, synth.BF16, synth.BF16,
                       synth.GATE_SOFTMAX, hidden="chain", rho=0.5),
     synth.TINY,
 ]
