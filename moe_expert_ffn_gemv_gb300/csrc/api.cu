@@ -158,9 +158,10 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
       act = S.h16;
       if (!early_shared) e = launch_act_scale(h, n, L.d, S, stream);
     }
-    // One 8-token MMA tile per pass over a work item: a segment with more
-    // tokens (the shared expert has all n) takes several passes over its
-    // weights.  Wider tiles (2 or 4 per pass) fit in registers, but their
+    // One 8-token mma.sync tile per pass over a work item.  A BF16 segment of
+    // more tokens runs on tcgen05 CTAs, all its tokens in one pass (P.wide);
+    // an E4M3 one (the shared expert at n > 8) takes one pass per 8 tokens.
+    // Wider mma.sync tiles (2 or 4 per pass) fit in registers, but their
     // activation rows leave the ring 3 or 4 stages, and they measured slower
     // than the extra passes.
     const int n_tiles = 1;
@@ -168,7 +169,12 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.T = T;
     P.err = err;
     P.timeout_ns = timeout_ns(L);
-    P.early_shared = early_shared && plan != nullptr;
+    // segments of more than 8 tokens on tcgen05 (BF16, deduplicating, n > 8)
+    P.wide = (!fp8 && plan != nullptr && n > 8) ? 1 : 0;
+    P.aperm = wsb + ws.aperm;
+    // phase 1: all n hidden rows in one box
+    if (P.wide && e == cudaSuccess) e = encode_act_map(&P.act_map[0], h, n, L.d, (n + 15) & ~15);
+    P.early_shared = early_shared && plan != nullptr && !P.wide;
     P.ready = P.early_shared ? ready : nullptr;
     int32_t *ashift = reinterpret_cast<int32_t *>(wsb + ws.ashift);
     P.hshift = S.hshift;
@@ -199,6 +205,9 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.row_blocks = L.d / 64;
     P.act = wsb + ws.inter;
     P.out = wsb + ws.yslot;
+    // phase 2: boxes of 16, 32, 48 or 64 rows of aperm
+    for (int j = 0; j < 4 && P.wide && e == cudaSuccess; ++j)
+      e = encode_act_map(&P.act_map[j], P.aperm, slots, L.inter, 16 * (j + 1));
     if (e == cudaSuccess) e = launch_expert_tc(fp8, 2, n_tiles, P, sms, stream);
   }
   if (e == cudaSuccess)

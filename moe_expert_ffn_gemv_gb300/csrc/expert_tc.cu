@@ -58,6 +58,8 @@
 // Every wait is bounded; on time-out the kernel records MOE_ERR_TIMEOUT in the
 // workspace error word, keeps its barrier structure, lets its own copies land
 // and returns.
+#include <mutex>
+
 #include "moe_common.cuh"
 #include "kernels.h"
 
@@ -141,6 +143,7 @@ struct LocalTables {
   const int16_t *tab;   // [n*k]    dedup: perm; per-slot: ids (-1: out of range)
   const int *U;         // U, in shared memory (read once the plan is there)
   int n, k, n_experts, n_shared, dedup;
+  int wide_m;           // segments of more tokens go to the tcgen05 CTAs (wide_cta)
 
   __device__ int n_segments() const { return dedup ? *U + n_shared : n * k + n_shared * n; }
   // segments whose work items are known before the plan is read
@@ -193,11 +196,15 @@ struct LocalTables {
 struct Cursor {
   int item, rb, grp, ks, groups;
   int u, seg_first, seg_items;  // segment, its first item, its items
+  int stride;                   // CTAs walking these items
   Seg sg;
 };
 
-__device__ __forceinline__ void cursor_start(Cursor &c) {
-  c.item = blockIdx.x;
+// CTA `first` of `stride` (the CTAs that run this path; the others, if any,
+// run the segments of more than T.wide_m tokens on tcgen05).
+__device__ __forceinline__ void cursor_start(Cursor &c, int first, int stride) {
+  c.item = first;
+  c.stride = stride;
   c.u = -1;
   c.seg_first = 0;
   c.seg_items = 0;
@@ -228,6 +235,10 @@ __device__ __forceinline__ bool cursor_item(Cursor &c, const LocalTables &T, int
       c.seg_items = 0;
       continue;
     }
+    if (c.sg.m > T.wide_m) {  // a tcgen05 CTA's
+      c.seg_items = 0;
+      continue;
+    }
     c.groups = (c.sg.m + TOK - 1) / TOK;
     c.seg_items = row_blocks * c.groups;
   }
@@ -238,12 +249,368 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
                                             int kstages, Ensure &ensure, int32_t *err,
                                             bool report) {
   if (++c.ks < kstages) return true;
-  c.item += gridDim.x;
+  c.item += c.stride;
   return cursor_item<TOK>(c, T, row_blocks, ensure, err, report);
 }
 
-template <bool FP8, int PHASE, int NT>
-__global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P) {
+// ------------------------------------------------------------- wide CTAs
+//
+// A segment of more than WIDE_M tokens (a popular routed expert in a
+// correlated draft tree, identical tokens, a shared expert at n > 8) would
+// stream its weights through the mma.sync path once per 8 tokens.  With BF16
+// weights it runs instead on the 5th-generation tensor cores, on CTAs of its
+// own (the first W of the grid), so that each weight row crosses the SM once
+// per pass:
+//   - a work item is (segment, row pair): 128 weight rows, the packed tiles
+//     of row blocks 2p and 2p + 1, against all m <= 64 tokens of the segment;
+//   - a stage is one 128-byte column of K: the two tiles' 8 KB columns (one
+//     bulk copy each, warp 0) are the A operand as they are (the packed BF16
+//     tiles are in the 128-byte swizzled K-major layout); B is one 2-D TMA
+//     box of that column (warp 1, the tensor map swizzling it as the MMA
+//     reads it): in phase 1 the hidden rows of all n tokens (the MMA runs
+//     every token and the epilogue keeps the segment's: rows of h are
+//     contiguous, the segment's tokens are not), in phase 2 the segment's
+//     rows of aperm, where phase 1 wrote them in plan order;
+//   - warp 8 allocates 128 tensor-memory columns (two accumulators of up to
+//     64 columns) and one of its threads issues tcgen05.mma (M = 128, N = n
+//     (phase 1) or m (phase 2) rounded up to 16, K = 16; four a stage),
+//     committing each stage's slot back to the producers and each finished
+//     item to the epilogue;
+//   - warps 4-7 read the accumulator rows of their lane quarter with
+//     tcgen05.ld.  Phase 1: the gate warp and the up warp of a tile put
+//     their sums in shared memory and share out a = silu(g)*u of the
+//     segment's tokens (a short loop over the m tokens, not one unrolled
+//     over all n columns: under the bulk-copy traffic each cold stretch of
+//     code costs about a microsecond to fetch), then write aperm in 16-byte
+//     pieces.  Phase 2 writes the per-slot output rows, also transposed
+//     through shared memory into 16-byte stores (each store instruction
+//     costs ~0.1-0.3 us under that traffic; one 4-byte store a column and
+//     lane held the first items up for 4-19 us).
+// W is the split of the grid with the shortest modelled makespan, a wide
+// item costing W_ITEM_COST hundredths of a narrow one: measured, a tensor-
+// memory CTA moves its (twice as large) items ~1.5x slower per byte than a
+// narrow CTA, with fewer weight bytes in flight (the B box shares the ring).
+// Every wait is bounded; after a time-out the warps keep walking their items
+// without waiting, so that all of them reach the final barrier, and the
+// tensor memory is freed only after every issued MMA has completed.
+constexpr int WIDE_M = 8;
+constexpr int W_A_BYTES = 16384;  // 128 rows x 128 bytes of K
+// Shared memory: the ring, then the epilogue's buffers, in what the narrow
+// kernel's layout leaves below its barriers (less 1 KB for the alignment).
+// A ring slot is the A operand and a B box of up to pad16(n) rows of 128
+// bytes; as many slots as fit (at most W_MAX_STAGES) keep 110-180 KB of
+// weights in flight, as the mma.sync CTAs do (160 KB).
+constexpr int W_MAX_STAGES = 12;
+// the modelled cost of a wide item, in hundredths of a narrow item's (the
+// best of 200-500 on Qwen3/OLMoE-shaped trees of 12-64 tokens)
+constexpr int W_ITEM_COST = 300;
+constexpr int W_AVAIL =
+    int(n_stages<false, 1>() * size_t(slot_bytes<false, 1>()) + n_red_bufs<false, 1>() * red_bytes<1>()) -
+    1024;
+// Epilogue buffers.  Phase 1, for each pair of warps (gate rows, up rows of
+// one tile): the gate and the up sums [pad16(n) tokens][32 rows] fp32, the
+// bf16 rows of a [m <= 64][32] and the segment's tokens [64] int16.
+// Phase 2: each warp's output staging, 32 columns x 32 rows of fp32.
+__host__ __device__ constexpr int wide_pair_bytes(int ncol) { return ncol * 32 * 4 * 2 + 64 * 32 * 2 + 128; }
+__host__ __device__ constexpr int wide_epi_bytes(int phase, int ncol) {
+  return phase == 1 ? 2 * wide_pair_bytes(ncol) : 4 * 32 * 32 * 4;
+}
+static_assert(W_AVAIL - wide_epi_bytes(1, 64) >= 4 * (W_A_BYTES + 64 * 128), "wide ring under 4 stages");
+constexpr uint32_t W_TMEM_COLS = 128;
+constexpr int W_PRODUCER = 0, W_BWARP = 1, W_EPI0 = 4, W_MMA = 8;
+
+// Wide item sequence of one CTA: items numbered segment by segment (wide
+// segments only), row pair innermost; CTA b of W takes items b, b + W, ...
+struct WideCursor {
+  int item, stride, u, first, count, p;
+  Seg sg;
+};
+
+__device__ __forceinline__ bool wide_next(WideCursor &c, const LocalTables &T, int pairs) {
+  while (c.item >= c.first + c.count) {
+    c.first += c.count;
+    c.u += 1;
+    if (c.u >= T.n_segments()) return false;
+    c.sg = T.segment(c.u);
+    c.count = (c.sg.expert != -2 && c.sg.m > T.wide_m) ? pairs : 0;
+  }
+  c.p = c.item - c.first;
+  return true;
+}
+
+template <int PHASE>
+__device__ __forceinline__ void wide_cta(const TcParams &P, const LocalTables &T, uint8_t *dyn,
+                                      int W, volatile int *abort_flag) {
+  __shared__ uint64_t wfull[W_MAX_STAGES], wempty[W_MAX_STAGES], tfull[2], tempty[2], wdone;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 128-byte swizzled operands start on 1024-byte boundaries
+  uint8_t *base = dyn + ((1024 - (smem_u32(dyn) & 1023)) & 1023);
+  // slot = A + a B box of pad16(n) rows (phase 2's boxes, pad16(m), are no larger)
+  const int ncol = (T.n + 15) & ~15;
+  const int wslot = W_A_BYTES + ncol * 128;
+  const int WS = min(W_MAX_STAGES, (W_AVAIL - wide_epi_bytes(PHASE, ncol)) / wslot);
+  uint8_t *epi = base + WS * wslot;  // the epilogue's buffers
+  const int kst = P.kdim / 64;  // 128-byte columns of K
+  const int64_t rb_bytes = int64_t(ROWS) * P.kdim * 2;
+  const int pairs = (P.row_blocks + 1) / 2;
+  const uint64_t limit = P.timeout_ns;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WS; ++s) {
+      mbar_init(&wfull[s], 2);  // the A and B warps' arrivals, with their copies' bytes
+      mbar_init(&wempty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(&wdone, 1);
+    fence_barrier_init();
+  }
+  if (warp == W_MMA) tmem_alloc(&tmem_slot, W_TMEM_COLS);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+  };
+  WideCursor cur;
+  cur.item = blockIdx.x;
+  cur.stride = W;
+  cur.u = -1;
+  cur.first = 0;
+  cur.count = 0;
+
+  if (warp == W_PRODUCER) {
+    // ------------------------------------------------ A: two tiles' columns
+    const uint64_t policy = policy_evict_first();
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && wide_next(cur, T, pairs)) {
+      const uint8_t *ebase =
+          cur.sg.expert >= 0 ? P.w + int64_t(cur.sg.expert) * P.expert_stride : P.w_sh;
+      const int rb0 = 2 * cur.p;
+      const bool two = rb0 + 1 < P.row_blocks;  // phase 2 may end on a single tile
+      for (int q = 0; q < kst; ++q, ++it) {
+        const int s = it % WS;
+        const uint32_t round = it / WS;
+        if (round > 0 && !mbar_wait_bounded(&wempty[s], (round - 1) & 1, limit)) {
+          ok = false;
+          break;
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *a = base + s * wslot;
+          mbar_arrive_expect_tx(&wfull[s], two ? 16384u : 8192u);
+          bulk_g2s(a, ebase + rb0 * rb_bytes + int64_t(q) * 8192, 8192, &wfull[s], policy);
+          if (two)
+            bulk_g2s(a + 8192, ebase + (rb0 + 1) * rb_bytes + int64_t(q) * 8192, 8192, &wfull[s],
+                     policy);
+        }
+        __syncwarp();
+      }
+      cur.item += cur.stride;
+    }
+    if (!ok) fail();
+    // let every copy this warp issued land before the CTA may exit
+    const uint32_t first = it > uint32_t(WS) ? it - WS : 0;
+    for (uint32_t j = first; j < it; ++j)
+      if (!mbar_wait_bounded(&wfull[j % WS], (j / WS) & 1, DRAIN_LIMIT_NS)) {
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+        break;
+      }
+  } else if (warp == W_BWARP) {
+    // ------------------------------- B: one TMA box of the column a stage
+    // Phase 2 reads phase 1's aperm, so it waits for phase 1 first.  Row t of
+    // a box lands at t * 128 from a 1024-byte boundary, where the map's
+    // 128-byte swizzle puts its chunk j at position j ^ (t % 8).  Rows past
+    // the segment's m (phase 2) belong to the next segment or arrive as
+    // zeros: they only reach accumulator columns that nothing reads.
+    if (PHASE == 2) pdl_wait();
+    uint32_t it = 0;
+    bool ok = true;
+    const int nk = T.n * T.k;
+    while (ok && wide_next(cur, T, pairs)) {
+      const int nb = PHASE == 1 ? (T.n + 15) & ~15 : (cur.sg.m + 15) & ~15;  // rows of the box
+      const void *map = &P.act_map[PHASE == 1 ? 0 : nb / 16 - 1];
+      const int y0 = PHASE == 1 ? 0 : cur.sg.expert == -1 ? nk : cur.sg.first;
+      for (int q = 0; q < kst; ++q, ++it) {
+        const int s = it % WS;
+        const uint32_t round = it / WS;
+        if (round > 0 && !mbar_wait_bounded(&wempty[s], (round - 1) & 1, limit)) {
+          ok = false;
+          break;
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *b = base + s * wslot + W_A_BYTES;
+          mbar_arrive_expect_tx(&wfull[s], uint32_t(nb) * 128);
+          tma_load_2d(b, map, q * 64, y0, &wfull[s]);
+        }
+        __syncwarp();
+      }
+      cur.item += cur.stride;
+    }
+    if (!ok) fail();
+    // let every copy this warp issued land before the CTA may exit
+    const uint32_t first = it > uint32_t(WS) ? it - WS : 0;
+    for (uint32_t j = first; j < it; ++j)
+      if (!mbar_wait_bounded(&wfull[j % WS], (j / WS) & 1, DRAIN_LIMIT_NS)) {
+        if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
+        break;
+      }
+  } else if (warp == W_MMA) {
+    // ----------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      uint32_t it = 0, ic = 0;
+      bool ok = true, issued = false;
+      while (ok && wide_next(cur, T, pairs)) {
+        const uint32_t idesc =
+            umma_idesc_bf16(128, PHASE == 1 ? (T.n + 15) & ~15 : (cur.sg.m + 15) & ~15);
+        const int acc = ic & 1;
+        const uint32_t tround = ic >> 1;
+        if (tround > 0 && !mbar_wait_bounded(&tempty[acc], (tround - 1) & 1, limit)) {
+          ok = false;
+          break;
+        }
+        tmem_fence_after_sync();
+        const uint32_t d = tmem + acc * 64;
+        for (int q = 0; q < kst; ++q, ++it) {
+          const int s = it % WS;
+          const uint32_t round = it / WS;
+          if (!mbar_wait_bounded(&wfull[s], round & 1, limit) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tmem_fence_after_sync();
+          const uint32_t a = smem_u32(base + s * wslot), b = a + W_A_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(d, umma_desc_sw128(a + 32 * k), umma_desc_sw128(b + 32 * k), idesc,
+                      q > 0 || k > 0);
+          umma_commit(&wempty[s]);
+          issued = true;
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        ++ic;
+        cur.item += cur.stride;
+      }
+      // every MMA issued has completed before tensor memory is freed
+      if (issued) {
+        umma_commit(&wdone);
+        if (!mbar_wait_bounded(&wdone, 0, DRAIN_LIMIT_NS)) record_error(P.err, MOE_ERR_TIMEOUT);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(P.err, MOE_ERR_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= W_EPI0 && warp < W_EPI0 + 4) {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp - W_EPI0;  // tensor-memory lane quarter
+    const int nk = T.n * T.k;
+    uint32_t ic = 0;
+    bool ok = true;
+    while (wide_next(cur, T, pairs)) {
+      const int m = cur.sg.m;
+      const int acc = ic & 1;
+      const uint32_t tround = ic >> 1;
+      if (ok && (*abort_flag || !mbar_wait_bounded(&tfull[acc], tround & 1, limit))) {
+        ok = false;
+        fail();
+      }
+      uint32_t v[64];
+      if (ok) {
+        tmem_fence_after_sync();
+        tmem_ld_x64(tmem + (uint32_t(32 * qd) << 16) + uint32_t(acc * 64), v);
+        tmem_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
+      if (PHASE == 1) {
+        // Accumulator column c is token c.  Quarters 0 and 1 hold the gate
+        // and the up rows of tile 0, quarters 2 and 3 those of tile 1; each
+        // pair meets in shared memory, where its two warps compute
+        // a = silu(g) * u of the segment's tokens (alternate tokens, a lane
+        // a row) and write them to aperm in 16-byte pieces.  The two pair
+        // barriers are passed on every item, also after a time-out.
+        const int pr = qd >> 1, up = qd & 1;
+        float *gs = reinterpret_cast<float *>(epi + pr * wide_pair_bytes(ncol));  // [ncol][32]
+        float *us = gs + ncol * 32;
+        __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(us + ncol * 32);  // [m][32]
+        int16_t *tok = reinterpret_cast<int16_t *>(ob + 64 * 32);               // [m]
+        if (ok) {
+          float *dst = up ? us : gs;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < ncol) dst[c * 32 + lane] = __uint_as_float(v[c]);
+          if (!up)
+            for (int i = lane; i < m; i += 32) tok[i] = int16_t(T.token(T.slot(cur.sg, i)));
+        }
+        if (pr) named_sync<2>(64); else named_sync<1>(64);
+        if (ok) {
+#pragma unroll 2
+          for (int i = up; i < m; i += 2) {
+            const int c = tok[i];
+            ob[i * 32 + lane] = __float2bfloat16_rn(silu_times(gs[c * 32 + lane], us[c * 32 + lane]));
+          }
+        }
+        if (pr) named_sync<2>(64); else named_sync<1>(64);
+        if (ok) {
+          // row i of the block: columns 64p + 32 pr .. + 31 of aperm row y0 + i
+          const int y0 = cur.sg.expert == -1 ? nk : cur.sg.first;
+          __nv_bfloat16 *a0 = static_cast<__nv_bfloat16 *>(P.aperm) + 64 * cur.p + 32 * pr;
+          for (int j = up * 32 + lane; j < 4 * m; j += 64) {
+            const int i = j >> 2, piece = j & 3;
+            *reinterpret_cast<uint4 *>(a0 + int64_t(y0 + i) * P.inter + piece * 8) =
+                *reinterpret_cast<const uint4 *>(ob + i * 32 + piece * 8);
+          }
+        }
+      } else if (ok) {
+        // rows 128p + 32qd .. +31 of the per-slot outputs, 32 columns at a time
+        // through this warp's 4 KB of the staging area
+        const int row0 = 128 * cur.p + 32 * qd;
+        float *st = reinterpret_cast<float *>(epi) + qd * 32 * 32;
+        float *out = static_cast<float *>(P.out);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (half * 32 < m) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) st[c * 32 + lane] = __uint_as_float(v[half * 32 + c]);
+            __syncwarp();
+            const int c = half * 32 + lane;
+            if (c < m && row0 < P.rows_total) {
+              const uint4 *src = reinterpret_cast<const uint4 *>(st + lane * 32);
+              uint4 *dst = reinterpret_cast<uint4 *>(out + int64_t(T.slot(cur.sg, c)) * P.rows_total + row0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) dst[j] = src[j];
+            }
+            __syncwarp();
+          }
+        }
+      }
+      ++ic;
+      cur.item += cur.stride;
+    }
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  if (warp == W_MMA) tmem_dealloc(tmem, W_TMEM_COLS);
+}
+
+template <bool FP8, int PHASE, int NT, bool WIDE>
+__global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const __grid_constant__ TcParams P) {
   constexpr int S = n_stages<FP8, NT>();
   constexpr int SLOT = slot_bytes<FP8, NT>();
   constexpr int RB = n_red_bufs<FP8, NT>();
@@ -369,7 +736,63 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
     __syncthreads();
   }
   LocalTables T{s_uniq, s_offs, s_tab, &s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared,
-                P.T.dedup};
+                P.T.dedup, (!FP8 && WIDE) ? WIDE_M : 0x7fffffff};
+  // BF16 deduplicating passes of more than WIDE_M tokens (never the early-start
+  // mode): the first W CTAs take the wide segments on tcgen05; every CTA
+  // computes the same W from the plan.
+  int W = 0;
+  if constexpr (!FP8 && WIDE) {
+    {
+      __shared__ int s_wide_ctas;
+      if (warp == 0) {
+        // narrow items (row block x token group) and wide items (row pairs)
+        int nb = 0, wi = 0;
+        const int ns = T.n_segments();
+        for (int u = lane; u < ns; u += 32) {
+          const Seg sg = T.segment(u);
+          if (sg.expert == -2 || sg.m <= 0) continue;
+          if (sg.m > WIDE_M) {
+            wi += (P.row_blocks + 1) / 2;
+          } else {
+            nb += ((sg.m + TOK - 1) / TOK) * P.row_blocks;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          nb += __shfl_xor_sync(0xffffffffu, nb, o);
+          wi += __shfl_xor_sync(0xffffffffu, wi, o);
+        }
+        // W: the split of the grid with the shortest modelled makespan, a
+        // wide item (two row blocks) costing W_ITEM_COST hundredths of a
+        // narrow one (one row block, one token group); each lane tries every
+        // 32nd W, the warp takes the best (ties to the smaller W)
+        const int G = gridDim.x;
+        int best_t = 0x7fffffff, best_w = 0;
+        if (wi > 0 && nb == 0) {
+          best_w = min(G, wi);
+        } else if (wi > 0) {
+          for (int w = 1 + lane; w < G && w <= wi; w += 32) {
+            const int t = max(W_ITEM_COST * ((wi + w - 1) / w), 100 * ((nb + (G - w) - 1) / (G - w)));
+            if (t < best_t) { best_t = t; best_w = w; }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const int ot = __shfl_xor_sync(0xffffffffu, best_t, o);
+          const int ow = __shfl_xor_sync(0xffffffffu, best_w, o);
+          if (ot < best_t || (ot == best_t && ow < best_w)) { best_t = ot; best_w = ow; }
+        }
+        if (lane == 0) s_wide_ctas = best_w;
+      }
+      __syncthreads();
+      W = s_wide_ctas;
+      if (int(blockIdx.x) < W) {
+        wide_cta<PHASE>(P, T, smem, W, &s_abort);
+        return;
+      }
+    }
+  }
+  const int n_first = int(blockIdx.x) - W, n_stride = int(gridDim.x) - W;
   // The plan gate of the warps other than the producer: a bounded wait on
   // tables_bar the first time a walk needs the plan.
   bool have_tables = !lazy;
@@ -413,7 +836,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       __syncwarp();
     }
     Cursor cur;
-    cursor_start(cur);
+    cursor_start(cur, n_first, n_stride);
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
     while (have) {
       const int b = ep % RB;
@@ -425,49 +848,99 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
         if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
       }
       if (!aborted) {
-        const float4 *rb_buf = red + b * RED_F4;
+        float4 *rb_buf = red + b * RED_F4;
         const int m_left = cur.sg.m - cur.grp * TOK;
         constexpr int MT_OUT = PHASE == 1 ? 2 : 4;
-        for (int q = lane; q < MT_OUT * NT * 32; q += 32) {
-          const int ln = q & 31, nt = (q >> 5) % NT, mt = q / (32 * NT);
+        const int gg = lane >> 2, cc = lane & 3;
+        // this lane's outputs: (row tile mt, N tile nt) = (j / NT, j % NT),
+        // rows mt*16 + gg (+8), columns nt*8 + 2cc (+1); the 8 warps'
+        // K-partials added in a fixed order
+        float res[MT_OUT * NT][4];
+#pragma unroll
+        for (int j = 0; j < MT_OUT * NT; ++j) {
+          const int nt = j % NT, mt = j / NT;
           if (nt * 8 >= m_left) continue;
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f), w4 = v;
 #pragma unroll
           for (int w = 0; w < CONSUMERS; ++w) {
-            const float4 x = rb_buf[((w * 4 + mt) * NT + nt) * 32 + ln];
+            const float4 x = rb_buf[((w * 4 + mt) * NT + nt) * 32 + lane];
             v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
             if (PHASE == 1) {
-              const float4 y = rb_buf[((w * 4 + mt + 2) * NT + nt) * 32 + ln];
+              const float4 y = rb_buf[((w * 4 + mt + 2) * NT + nt) * 32 + lane];
               w4.x += y.x; w4.y += y.y; w4.z += y.z; w4.w += y.w;
             }
           }
-          const int gg = ln >> 2, cc = ln & 3;
           const float vals[4] = {v.x, v.y, v.z, v.w};
           const float ups[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int row = mt * 16 + gg + (e >> 1) * 8;
-            const int col = nt * 8 + 2 * cc + (e & 1);
-            if (col >= m_left) continue;
-            const int slot = T.slot(cur.sg, cur.grp * TOK + col);
             if (PHASE == 1) {
+              // columns past the segment's tokens are left out (never stored)
               float gv = vals[e], uv = ups[e];
-              if (FP8) {
-                // the rows were scaled by 2^hshift: scale the sums back
-                const float back = pow2f(-s_hshift[T.token(slot)]);
-                gv *= back;
-                uv *= back;
+              const int col = nt * 8 + 2 * cc + (e & 1);
+              res[j][e] = 0.f;
+              if (col < m_left) {
+                if (FP8) {
+                  // the rows were scaled by 2^hshift: scale the sums back
+                  const float back = pow2f(-s_hshift[T.token(T.slot(cur.sg, cur.grp * TOK + col))]);
+                  gv *= back;
+                  uv *= back;
+                }
+                res[j][e] = silu_times(gv, uv);
               }
-              const float a = silu_times(gv, uv);
-              uint16_t *out =
-                  static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter + cur.rb * 32 + row;
-              *reinterpret_cast<__nv_bfloat16 *>(out) = __float2bfloat16_rn(a);
             } else {
-              float *out = static_cast<float *>(P.out) + int64_t(slot) * P.rows_total +
-                           cur.rb * ROWS + row;
-              // E4M3: a reached the MMA scaled by 2^ashift[slot]
-              *out = FP8 ? vals[e] * pow2f(-s_ashift[slot]) : vals[e];
+              res[j][e] = vals[e];
             }
+          }
+        }
+        // Through the buffer just read: [column][row] fp32, CS floats a
+        // column (a stride that puts the 32 lanes' writes in 32 banks), then
+        // each column's rows leave as 16-byte pieces: one store instruction
+        // in place of 8 (phase 1) or 16 (phase 2) of 2 or 4 bytes a lane,
+        // each of which costs ~0.1-0.3 us under the bulk-copy traffic.
+        constexpr int CS = PHASE == 1 ? 36 : 68;
+        float *st = reinterpret_cast<float *>(rb_buf);
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < MT_OUT * NT; ++j) {
+          const int nt = j % NT, mt = j / NT;
+          if (nt * 8 >= m_left) continue;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            st[(nt * 8 + 2 * cc + (e & 1)) * CS + mt * 16 + gg + (e >> 1) * 8] = res[j][e];
+        }
+        __syncwarp();
+        const int mcols = min(m_left, TOK);
+        if (PHASE == 1) {
+          // a column: rows rb*32 .. +31 of a, 4 pieces of 8 bf16
+          for (int q = lane; q < mcols * 4; q += 32) {
+            const int col = q >> 2, piece = q & 3;
+            const float4 lo = *reinterpret_cast<const float4 *>(st + col * CS + piece * 8);
+            const float4 hi = *reinterpret_cast<const float4 *>(st + col * CS + piece * 8 + 4);
+            const __nv_bfloat162 p0 = __floats2bfloat162_rn(lo.x, lo.y), p1 = __floats2bfloat162_rn(lo.z, lo.w);
+            const __nv_bfloat162 p2 = __floats2bfloat162_rn(hi.x, hi.y), p3 = __floats2bfloat162_rn(hi.z, hi.w);
+            uint4 o;
+            o.x = *reinterpret_cast<const uint32_t *>(&p0);
+            o.y = *reinterpret_cast<const uint32_t *>(&p1);
+            o.z = *reinterpret_cast<const uint32_t *>(&p2);
+            o.w = *reinterpret_cast<const uint32_t *>(&p3);
+            const int slot = T.slot(cur.sg, cur.grp * TOK + col);
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(P.out) + int64_t(slot) * P.inter +
+                                       cur.rb * 32 + piece * 8) = o;
+          }
+        } else {
+          // a column: rows rb*64 .. +63 of the slot's output, 16 pieces of 4
+          for (int q = lane; q < mcols * 16; q += 32) {
+            const int col = q >> 4, piece = q & 15;
+            float4 x = *reinterpret_cast<const float4 *>(st + col * CS + piece * 4);
+            const int slot = T.slot(cur.sg, cur.grp * TOK + col);
+            if (FP8) {
+              // E4M3: a reached the MMA scaled by 2^ashift[slot]
+              const float back = pow2f(-s_ashift[slot]);
+              x.x *= back; x.y *= back; x.z *= back; x.w *= back;
+            }
+            *reinterpret_cast<float4 *>(static_cast<float *>(P.out) + int64_t(slot) * P.rows_total +
+                                        cur.rb * ROWS + piece * 4) = x;
           }
         }
       }
@@ -587,7 +1060,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       }
     };
     Cursor cur;
-    cursor_start(cur);
+    cursor_start(cur, n_first, n_stride);
     bool have = cursor_item<TOK>(cur, T, P.row_blocks, load_plan, P.err, false);
     while (have) {
       const int s = it % S;
@@ -651,7 +1124,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       fence_proxy_async_global();
     }
     Cursor cur;
-    cursor_start(cur);
+    cursor_start(cur, n_first, n_stride);
     bool have = ok && cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, false);
     while (have) {
       const int s = it % S;
@@ -706,7 +1179,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
       for (int q = 0; q < 4; ++q) acc[mt][nt][q] = 0.f;
 
   Cursor cur;
-  cursor_start(cur);
+  cursor_start(cur, n_first, n_stride);
   bool have = cursor_item<TOK>(cur, T, P.row_blocks, await_tables, P.err, tid == 0);
 
   while (have) {
@@ -850,14 +1323,18 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const TcParams P)
   }
 }
 
-template <bool FP8, int PHASE, int NT>
+template <bool FP8, int PHASE, int NT, bool WIDE>
 cudaError_t launch_one(const TcParams &P, int grid, cudaStream_t stream) {
-  auto kern = expert_tc_kernel<FP8, PHASE, NT>;
+  auto kern = expert_tc_kernel<FP8, PHASE, NT, WIDE>;
   constexpr size_t smem = smem_bytes<FP8, NT>();
   // 227 KB per CTA, of which the static plan tables take under 6.5 KB
   // (E4M3 phase 2 adds its 2.1 KB table of slot exponents)
   static_assert(smem + 6656 + (FP8 && PHASE == 2 ? MAX_ALL_SLOTS : 0) <= 232448,
                 "the ring does not fit in shared memory");
+  // the wide CTAs' layout (W_AVAIL) stays below the ring's barriers (set up by every CTA)
+  static_assert(FP8 || size_t(W_AVAIL) + 1024 <= size_t(n_stages<FP8, NT>()) * slot_bytes<FP8, NT>() +
+                                                  n_red_bufs<FP8, NT>() * red_bytes<NT>(),
+                "the wide layout overlaps the ring's barriers");
   // the shared-memory opt-in is set once per device (the first call), so
   // later calls, e.g. under stream capture, only launch
   static unsigned long long configured = 0;
@@ -876,10 +1353,47 @@ cudaError_t launch_one(const TcParams &P, int grid, cudaStream_t stream) {
 template <bool FP8, int PHASE>
 cudaError_t launch_nt(const TcParams &P, int nt, int grid, cudaStream_t stream) {
   if (nt != 1) return cudaErrorInvalidValue;  // only the 8-token tile is built
-  return launch_one<FP8, PHASE, 1>(P, grid, stream);
+  // the tcgen05 CTAs are compiled into a kernel of their own, so that passes
+  // without them run the mma.sync code as it is
+  if constexpr (!FP8)
+    if (P.wide) return launch_one<FP8, PHASE, 1, true>(P, grid, stream);
+  return launch_one<FP8, PHASE, 1, false>(P, grid, stream);
 }
 
 }  // namespace
+
+cudaError_t encode_act_map(CUtensorMap *map, const void *act, int rows, int kdim, int box_rows) {
+  // cuTensorMapEncodeTiled from the driver, found once through the runtime
+  using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode fn = nullptr;
+  static cudaError_t found = cudaSuccess;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    found = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q);
+    if (found == cudaSuccess && (q != cudaDriverEntryPointSuccess || !p))
+      found = cudaErrorNotSupported;
+    fn = reinterpret_cast<Encode>(p);
+  });
+  if (found != cudaSuccess) return found;
+  // [rows][kdim] bf16, row stride kdim * 2 bytes (kdim % 64 == 0); boxes of
+  // 64 elements (128 bytes) x box_rows rows, swizzled 128 bytes as the MMA
+  // reads B; rows past the end arrive as zeros
+  const cuuint64_t dims[2] = {cuuint64_t(kdim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(kdim) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(act), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t launch_expert_tc(bool fp8, int phase, int n_tiles, const TcParams &P, int grid,
                              cudaStream_t stream) {

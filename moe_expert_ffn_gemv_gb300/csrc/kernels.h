@@ -1,6 +1,7 @@
 // kernels.h -- launchers of the library's kernels (internal; C++ linkage).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,7 +58,20 @@ struct TcParams {
   const int32_t *hshift;
   const int32_t *ashift;
   const uint32_t *acts;
+  // BF16 deduplicating pass of more than 8 tokens, not in the early-start
+  // mode: segments of more than 8 tokens run on tcgen05 CTAs (expert_tc.cu).
+  // Their activations come in 2-D TMA boxes of 64 elements x 16 (j + 1) rows
+  // through act_map[j] (128-byte swizzle): phase 1 the hidden states [n][d]
+  // (one map, all tokens), phase 2 `aperm` [slots][I], which phase 1 writes
+  // for these segments in plan order.
+  int32_t wide;
+  void *aperm;
+  CUtensorMap act_map[4];
 };
+
+// A tensor map of `rows` rows of `kdim` bf16 elements at `act` (kdim % 64 ==
+// 0), boxes of 64 elements x box_rows rows, 128-byte swizzle.
+cudaError_t encode_act_map(CUtensorMap *map, const void *act, int rows, int kdim, int box_rows);
 
 // Tensor-core expert FFN (BF16 weights, or E4M3 with fp32 block scales);
 // n_tiles = 8-token MMA tiles per pass (1, 2 or 4).

@@ -161,6 +161,19 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Two-dimensional TMA tensor copy global -> shared of the box at element
+// coordinates (x, y) of the tensor map (x, the innermost, a multiple of 16
+// bytes' worth of elements), completing its bytes on `bar`.  `map` is the
+// generic address of a tensor map in kernel parameter space.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Asks L2 to fetch [p, p + bytes) ahead of use, at normal priority (a hint;
 // p and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2(const void *p, uint64_t bytes) {
@@ -193,6 +206,105 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
+}
+
+// ---- tcgen05 (5th-generation tensor cores; accumulators in tensor memory)
+//
+// Shared-memory operand descriptor of a K-major tile in the 128-byte swizzled
+// layout: rows of 128 bytes, 8-row groups 1024 bytes apart (the stride
+// field), 16-byte chunk j of row r stored at position j ^ (r % 8), groups
+// starting on 1024-byte boundaries.  Fields: start address >> 4 (bits
+// 0-13), leading offset (unused by this layout, 1), stride offset >> 4
+// (bits 32-45), descriptor version 1 (bit 46), layout 2 = 128-byte swizzle
+// (bits 61-63).  A K step of 16 bf16 elements (32 bytes) inside the 128-byte
+// row advances the start address by 32.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  return uint64_t((smem_addr >> 4) & 0x3FFF) | (uint64_t(1) << 16) |
+         (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and
+// fp32 accumulators: D format (bits 4-5) 1 = f32, A format (7-9) and B
+// format (10-12) 1 = bf16, N >> 3 (17-22), M >> 4 (24-28).
+__device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate)));
+}
+
+// Arrives (once) on `bar` when every tcgen05 operation this thread issued
+// before has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole warp: allocate `cols` tensor-memory columns (a power of two >= 32),
+// the base address written to *slot; then give up the right to allocate more.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Whole warp.
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols)
+               : "memory");
+}
+
+// Whole warp: 64 consecutive 32-bit columns of the warp's 32 lanes (lane l
+// of the warp gets row (taddr lane) + l), then waits for the load.
+__device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]),
+        "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]),
+        "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]),
+        "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (tcgen05.mma operand reads, bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier ID (1..15) over `threads` threads (a multiple of 32).
+template <int ID>
+__device__ __forceinline__ void named_sync(int threads) {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(threads) : "memory");
 }
 
 // Four E4M3 bytes b0..b3 (b0 least significant) -> two f16x2 words:
@@ -247,8 +359,12 @@ __device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) 
 //   h16                [n_max][d] fp16: h[t] * 2^hshift[t]
 //   hshift             [n_max] int32
 //   ashift             [n_max*(k+n_shared)] int32
+//   BF16 weights only:
+//   aperm              [n_max*(k+n_shared)][I] bf16: a of the segments the
+//                      tcgen05 CTAs run, in plan order (row offs[u] + i for
+//                      slot perm[offs[u] + i]; the shared expert at n*k + t)
 struct Workspace {
-  size_t inter, yslot, h16, hshift, ashift, total;
+  size_t inter, yslot, h16, hshift, ashift, aperm, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -278,6 +394,8 @@ inline Workspace workspace_layout(const moe_layer_desc &L) {
   off += e4m3 ? align256(size_t(L.n_max) * 4) : 0;
   w.ashift = off;
   off += e4m3 ? align256(slots * 4) : 0;
+  w.aperm = off;
+  off += L.w_dtype == MOE_BF16 ? align256(slots * size_t(L.inter) * 2) : 0;
   w.total = off;
   return w;
 }
