@@ -79,7 +79,8 @@ def parse():
     p.add_argument("--rho", type=float, default=None, help="chain/tree correlation for the sweep")
     p.add_argument("--sigma", type=float, default=None, help="tree noise for the sweep")
     p.add_argument("--experts", type=int, default=None,
-                   help="routed experts of the layer (default 256); fewer make a small profiling case")
+                   help="routed experts of the layer (default: the shape's own); fewer make a "
+                        "small profiling case")
     return p.parse_args()
 
 
@@ -604,6 +605,9 @@ def run_sweep_only(args):
     from moe_expert_ffn_gemv_gb300 import binding as mv
     torch.cuda.set_device(0)
     cfg = synth.CONFIGS[args.sweep_config]
+    if args.experts:
+        from dataclasses import replace
+        cfg = replace(cfg, n_experts=args.experts, name=f"{cfg.name} ({args.experts} routed experts)")
     layer = synth.make_layer(cfg, seed=1, device="cuda")
     h_all = synth.make_hidden(cfg, 64, seed=3, device="cuda", rho=args.rho, sigma=args.sigma)
     eb = sum(mv.moe_expert_bytes(mv.make_desc(cfg, 64)))
