@@ -375,6 +375,7 @@ moe_status route_plan(const moe_layer_desc *desc, const void *router_w, const vo
       desc->gate, desc->n_shared, wb + sb, logits, ids, w, plan->hist, plan->uniq, plan->n_uniq,
       plan->offs, plan->perm, plan->union_bytes, budget, w_kept, routed_u, err,
       reinterpret_cast<unsigned int *>(wsb + WS_TICKET_OFFSET),
+      reinterpret_cast<unsigned int *>(wsb + WS_GROUP_TICKETS_OFFSET),
       signal_ready ? reinterpret_cast<unsigned int *>(wsb + WS_READY_OFFSET) : nullptr, S, st));
 }
 

@@ -127,7 +127,8 @@ cudaError_t launch_topk_gate(const float *logits, int n, int n_experts, int k, i
                              int32_t *ids, float *w, cudaStream_t stream);
 
 // Router scores + top-k + gate + union plan in one launch; `counter` is a
-// zeroed device word that the kernel leaves zeroed.  budget >= 0: the
+// zeroed device word and `group_counter` (n + 7) / 8 of them, all left
+// zeroed by the kernel.  budget >= 0: the
 // budgeted plan (w_kept written, routed_u if not NULL); budget < 0: none.
 // `ready` (or null): set to 1 with release semantics once the plan is written.
 // S.acts (or null): bf16 activations only; the launch also writes the E4M3
@@ -137,8 +138,8 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
                               int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-                              unsigned int *counter, unsigned int *ready, const ActScaleOut &S,
-                              cudaStream_t stream);
+                              unsigned int *counter, unsigned int *group_counter,
+                              unsigned int *ready, const ActScaleOut &S, cudaStream_t stream);
 
 // Expert union and slot permutation (one CTA).
 cudaError_t launch_union_plan(const int32_t *ids, int n_slots, int n_experts, int n_shared,

@@ -347,7 +347,8 @@ __device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) 
 
 // Layout of the caller's workspace (all offsets 256-byte aligned):
 //   [0, 256)           header: int32 error word at byte 0, the fused
-//                      route + plan kernel's ticket counter at byte 64,
+//                      route + plan kernel's ticket counters at byte 64
+//                      and at bytes 128 .. 159 (one an 8-token group),
 //                      moe_verify_pass's plan-ready flag at byte 72 and its
 //                      scaled-rows counter at byte 76
 //   inter              [n_max*(k+n_shared)][I] intermediate a = silu(g)*u
@@ -370,6 +371,10 @@ struct Workspace {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr size_t WS_TICKET_OFFSET = 64;
+// The fused route + plan kernel's ticket counters of the 8-token groups
+// (n_max / 8 <= 8 of them), at bytes 128 .. 159; each is back at zero when
+// the kernel ends.
+constexpr size_t WS_GROUP_TICKETS_OFFSET = 128;
 // The plan-ready flag of moe_verify_pass: raised by its plan kernel once the
 // plan is written, read by its first expert kernel, cleared by its combine.
 constexpr size_t WS_READY_OFFSET = 72;

@@ -128,10 +128,13 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float *__restrict_
 
 // Router scores, top-k + gate and the union plan in one launch.  Every CTA
 // computes its (expert, 8-token) scores as router_scores_kernel does, then
-// takes a ticket; the CTA that takes the last ticket (so all scores are
-// written) runs the top-k of every token (one warp per token) and then
-// union_plan_block (BUDGET: the budgeted plan), and resets the ticket
-// counter for the next call.  With `A.acts` set, the grid has one more CTA
+// takes a ticket of its 8-token group; the CTA that takes the group's last
+// ticket (so the group's scores are all written) runs the top-k of the
+// group's tokens, one warp a token, and takes a ticket of the kernel; the
+// CTA that takes the kernel's last ticket (so every token is ranked) runs
+// union_plan_block (BUDGET: the budgeted plan).  Each counter is reset by
+// the CTA that took its last ticket, for the next call.  (One CTA ranking
+// all n tokens, 8 warps, took ~20 us of a 64-token pass.)  With `A.acts` set, the grid has one more CTA
 // column (blockIdx.x == n_experts): it writes the fp16 rows of its 8 tokens
 // (act_scale_block) and counts them in *A.acts with release semantics, for
 // the E4M3 expert kernel that starts before this kernel ends.  It takes no
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
     int gate, int n_shared, int64_t expert_bytes, float *logits, int32_t *ids, float *w,
     int32_t *hist, int32_t *uniq, int32_t *n_uniq, int32_t *offs, int32_t *perm,
     int64_t *union_bytes, int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-    unsigned int *counter, unsigned int *ready, ActScaleOut A) {
+    unsigned int *counter, unsigned int *group_counter, unsigned int *ready, ActScaleOut A) {
   pdl_trigger();  // the expert kernel behind this one may launch (it waits for the plan)
   if (blockIdx.x < unsigned(n_experts)) {
     router_scores_cta(wg, h, n, d, n_experts, logits);
@@ -162,17 +165,30 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // this CTA's scores before its ticket
-    const unsigned int ticket = atomicAdd(counter, 1u);
-    s_last = ticket == unsigned(n_experts) * gridDim.y - 1;  // the router CTAs
+    const unsigned int ticket = atomicAdd(group_counter + blockIdx.y, 1u);
+    s_last = ticket == unsigned(n_experts) - 1;  // the group's router CTAs
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  for (int t = warp; t < n; t += n_warps)
-    topk_gate_warp(logits + int64_t(t) * n_experts, n_experts, k, gate, ids + int64_t(t) * k,
-                   w + int64_t(t) * k);
-  __syncthreads();  // ids and weights of all tokens visible to the whole CTA
+  {
+    // the group's tokens, one warp each (a router CTA has at least 8 warps)
+    const int warp = threadIdx.x >> 5;
+    const int t = blockIdx.y * TOKENS_PER_CTA + warp;
+    if (warp < TOKENS_PER_CTA && t < n)
+      topk_gate_warp(logits + int64_t(t) * n_experts, n_experts, k, gate, ids + int64_t(t) * k,
+                     w + int64_t(t) * k);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    group_counter[blockIdx.y] = 0u;
+    __threadfence();  // this group's ids and weights before its ticket
+    const unsigned int ticket = atomicAdd(counter, 1u);
+    s_last = ticket == gridDim.y - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
   __shared__ PlanSmem S;
   if constexpr (BUDGET) {
     __shared__ BudgetSmem B;
@@ -224,8 +240,8 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
                               float *logits, int32_t *ids, float *w, int32_t *hist, int32_t *uniq,
                               int32_t *n_uniq, int32_t *offs, int32_t *perm, int64_t *union_bytes,
                               int budget, float *w_kept, int32_t *routed_u, int32_t *err,
-                              unsigned int *counter, unsigned int *ready, const ActScaleOut &S,
-                              cudaStream_t stream) {
+                              unsigned int *counter, unsigned int *group_counter,
+                              unsigned int *ready, const ActScaleOut &S, cudaStream_t stream) {
   // E4M3 rows are written only beside bf16 activations (the only kind E4M3 weights take)
   const bool scale = S.acts != nullptr && bf16;
   dim3 grid(n_experts + (scale ? 1 : 0), (n + TOKENS_PER_CTA - 1) / TOKENS_PER_CTA);
@@ -238,7 +254,7 @@ cudaError_t launch_route_plan(bool bf16, const void *router_w, const void *h, in
   if (!scale) Sx.acts = nullptr;
 #define MOE_ROUTE_PLAN_ARGS                                                                  \
   n, d, n_experts, k, gate, n_shared, expert_bytes, logits, ids, w, hist, uniq, n_uniq, offs, \
-      perm, union_bytes, budget, w_kept, routed_u, err, counter, ready, Sx
+      perm, union_bytes, budget, w_kept, routed_u, err, counter, group_counter, ready, Sx
   if (budget < 0) {
     if (bf16)
       route_plan_kernel<__nv_bfloat16, false><<<grid, threads, 0, stream>>>(wb, hb,

@@ -183,8 +183,8 @@ __device__ __forceinline__ bool budget_beats(unsigned long long a, int e, unsign
 // (contribution descending, id ascending); the plan is rebuilt over the kept
 // slots only, and w_kept[p] = w[p] for a kept slot, 0 for a dropped one (or
 // an invalid id).  routed_u (may be NULL) receives U before the cut.
-// `ids` and `w` may be written by this block just before (after a
-// __syncthreads), so they are read with plain loads.
+// `ids` and `w` may have been written by other CTAs of the same kernel (the
+// fused route + plan kernel, behind its ticket), so they are read through L2.
 template <bool BUDGET>
 __device__ __forceinline__ void union_plan_block(
     PlanSmem &S, BudgetSmem *B, const int32_t *ids, const float *w, int n_slots, int n_experts,
@@ -195,10 +195,10 @@ __device__ __forceinline__ void union_plan_block(
   if (tid < 256) S.hist[tid] = 0;
   __syncthreads();
   for (int p = tid; p < n_slots; p += blockDim.x) {
-    const int e = ids[p];
+    const int e = __ldcg(ids + p);
     const bool ok = e >= 0 && e < n_experts;
     S.ids[p] = ok ? e : -1;
-    if constexpr (BUDGET) B->w[p] = w[p];
+    if constexpr (BUDGET) B->w[p] = __ldcg(w + p);
     if (ok) atomicAdd(&S.hist[e], 1);
     else record_error(err, MOE_ERR_DEVICE_INPUT);
   }
