@@ -45,8 +45,9 @@ METRIC = "µs per MoE verify pass and union-byte HBM GB/s (% of GB300 peak) vs n
 WORKLOAD = "deepseek-v3-shaped fp8-e4m3 moe layer, n=8 draft-tree tokens (rho=0.6), dedup verify pass"
 NOMINAL_HBM_GBS = (7900.0, 8000.0)  # GB300 HBM3e nominal: 7.9 TB/s, "~8 TB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_PASS = 4  # route + top-k + plan (fused; E4M3: + fp16 rows), gate/up, down, combine
-KERNELS_PER_DEDUP_CALL = 4  # E4M3 fp16 rows, gate/up, down, combine
+# E4M3: route + top-k + plan (fused, + the fp16 rows of h), gate/up, fp16 rows of a, down, combine
+KERNELS_PER_PASS = 5
+KERNELS_PER_DEDUP_CALL = 5  # E4M3: fp16 rows of h, gate/up, fp16 rows of a, down, combine
 
 
 def parse():

@@ -209,10 +209,11 @@ moe_status moe_union_plan(const moe_layer_desc *desc, const int32_t *ids,
                           moe_stream_t stream);
 
 /* moe_route_topk followed by moe_union_plan, in one kernel launch: the
- * router CTAs write the scores; the last CTA to finish selects the top-k of
- * every token, gates, and builds the plan.  Same outputs, bit for bit.
+ * router CTAs write the scores; the last CTA to finish each group of 8
+ * tokens selects their top-k and gates, and the last of those builds the
+ * plan.  Same outputs, bit for bit.
  *   workspace  a workspace initialised by moe_workspace_init (only its
- *              256-byte header is used: the error word, and a ticket counter
+ *              256-byte header is used: the error word, and ticket counters
  *              the kernel leaves at zero); ws_bytes >= 256.  Calls sharing a
  *              workspace must not overlap on the GPU.
  * n may be 0: the plan becomes empty (U = 0). */
