@@ -173,7 +173,12 @@ __device__ __forceinline__ bool budget_beats(unsigned long long a, int e, unsign
 //   1. histogram with shared-memory atomics;
 //   2. plan_scan: the used experts in ascending order and their offsets;
 //   3. stable scatter: slot p goes to offs[ids[p]] + (earlier slots with the
-//      same id), so slots stay ascending inside a group;
+//      same id), so slots stay ascending inside a group: one warp walks the
+//      slots in order, 32 at a time; __match_any_sync gives each slot its
+//      rank among the chunk's slots of the same expert, and a running count
+//      per expert (in shared memory, over the offsets) carries it across
+//      chunks.  (Counting the earlier slots of each slot was O(slots^2)
+//      compares: ~1,000 a thread at 512 slots.);
 //   4. U and the union bytes (U + n_shared) * expert bytes.
 // BUDGET: at most `budget` routed experts are kept (MoE-Spec's per-layer
 // expert cap).  The weights are staged in shared memory with the ids.  When
@@ -209,13 +214,24 @@ __device__ __forceinline__ void union_plan_block(
   if (BUDGET && tid == 0 && routed_u) *routed_u = S.n_uniq;
   int32_t *group = cut ? B->perm : perm;  // where the full grouping goes
   __syncthreads();
-  for (int p = tid; p < n_slots; p += blockDim.x) {
-    const int id = S.ids[p];
-    if (id < 0) continue;
-    int before = 0;
-    for (int q = 0; q < p; ++q) before += S.ids[q] == id;
-    group[S.offs[id] + before] = p;
+  if (tid < 32) {
+    // S.offs[e] runs on as expert e's next free position (restored below)
+    const unsigned lt = (1u << tid) - 1u;
+    for (int c = 0; c < n_slots; c += 32) {
+      const int p = c + tid;
+      const int id = p < n_slots ? S.ids[p] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, id);
+      const int pos = id >= 0 ? S.offs[id] + __popc(peers & lt) : 0;
+      __syncwarp();
+      if (id >= 0) {
+        group[pos] = p;
+        if ((peers & lt) == 0u) S.offs[id] += __popc(peers);  // the group's first lane
+      }
+      __syncwarp();
+    }
   }
+  __syncthreads();
+  if (tid < 256) S.offs[tid] = x.off;  // the scan's offsets again
   if constexpr (BUDGET) {
     if (cut) {
       __syncthreads();  // the grouping in B->perm is complete
