@@ -205,24 +205,31 @@ def clocks_rejected(clocks) -> bool:
 
 def traffic_from_profile():
     """DRAM bytes per dedup call from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+    taken on the current sources of the kernels that call runs (else None)."""
     path = os.path.join(ROOT, "profiles", "dedup_dsv3_fp8_n8.md")
     try:
         with open(path) as f:
             for line in f:
                 if line.startswith("traffic_json:"):
                     j = json.loads(line.split(":", 1)[1])
-                    if j.get("csrc_sha256") == csrc_hash():
+                    if j.get("dedup_kernels_sha256") == csrc_hash(DEDUP_KERNEL_SOURCES):
                         return j.get("dram_bytes_per_dedup_call")
     except Exception:
         pass
     return None
 
 
-def csrc_hash() -> str:
+# The sources of the kernels a moe_verify_dedup call runs (and the layout
+# they read): what a recorded DRAM-traffic figure for that call depends on.
+DEDUP_KERNEL_SOURCES = ("act_scale.cu", "act_scale.cuh", "combine.cu", "expert_tc.cu", "kernels.h",
+                        "moe_common.cuh", "pack.cu")
+
+
+def csrc_hash(names=None) -> str:
+    """Hash of the kernel sources (all of csrc/, or the named files)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "moe_expert_ffn_gemv_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in sorted(names or os.listdir(d)):
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
