@@ -39,20 +39,28 @@ def _pass(mv, layer, h, n, timeout_us):
     return y, vl.last_error()
 
 
-def test_tiny_wait_limit_ends_cleanly_then_normal_call_is_right(mv):
-    layer = synth.make_layer(SMALL, seed=4).to("cuda")
-    h = synth.make_hidden(SMALL, 8, seed=5)
+# A BF16 layer with a shared expert at 12 tokens: the shared expert's segment
+# (and any routed one of more than 8 tokens) runs on the tcgen05 CTAs.
+WIDE = synth.LayerConfig("bf16-wide-fault", 512, 12, 3, 192, synth.BF16, synth.BF16,
+                         synth.GATE_SOFTMAX_RENORM, n_shared=1, hidden="tree_add", sigma=0.3)
+
+
+@pytest.mark.parametrize("cfg,n", [(SMALL, 8), (WIDE, 12)], ids=["fp8-n8", "bf16-tcgen05-n12"])
+def test_tiny_wait_limit_ends_cleanly_then_normal_call_is_right(mv, cfg, n):
+    layer = synth.make_layer(cfg, seed=4).to("cuda")
+    h = synth.make_hidden(cfg, n, seed=5)
     hd = h.cuda()
     # a 1 microsecond limit: waits may run out; the call must end with OK or
-    # TIMEOUT, never hang
+    # TIMEOUT, never hang (on the tcgen05 CTAs too: every wait bounded, the
+    # tensor memory freed after the issued MMAs complete)
     for _ in range(3):
-        _, status = _pass(mv, layer, hd, 8, 1)
+        _, status = _pass(mv, layer, hd, n, 1)
         assert status in (mv.MOE_OK, mv.MOE_ERR_TIMEOUT)
-    y, status = _pass(mv, layer, hd, 8, 0)
+    y, status = _pass(mv, layer, hd, n, 0)
     assert status == mv.MOE_OK
     L = oracle_layer(layer.to("cpu"))
     _, _, _, y_ref = oracle.verify(L, np_bytes(h))
-    assert rel_err(y, y_ref) <= TOL[SMALL.wtype]
+    assert rel_err(y, y_ref) <= TOL[cfg.wtype]
 
 
 def test_out_of_range_ids_are_reported_by_both_engines(mv):
@@ -99,14 +107,14 @@ MALFORMED = ["uniq_out_of_range", "perm_out_of_range", "u_too_large", "offs_decr
              "offs_past_slots", "offs_negative"]
 
 
-@pytest.mark.parametrize("cfg", [SMALL, synth.shrink(synth.OLMOE, 512, 128), synth.TINY],
-                         ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg,n", [(SMALL, 6), (synth.shrink(synth.OLMOE, 512, 128), 6),
+                                   (synth.TINY, 6), (WIDE, 12)],
+                         ids=["fp8", "bf16", "f32", "bf16-tcgen05-n12"])
 @pytest.mark.parametrize("kind", MALFORMED)
-def test_a_malformed_caller_plan_is_reported_not_followed(mv, cfg, kind):
+def test_a_malformed_caller_plan_is_reported_not_followed(mv, cfg, n, kind):
     # moe_verify_dedup takes any plan from its caller: the expert kernels
     # check it before using its indices and report MOE_ERR_DEVICE_INPUT
     layer = synth.make_layer(cfg, seed=4).to("cuda")
-    n = 6
     h = synth.make_hidden(cfg, n, seed=5).cuda()
     vl = mv.VerifyLayer(layer, n)
     vl.route(h, n)
