@@ -169,11 +169,21 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.T = T;
     P.err = err;
     P.timeout_ns = timeout_ns(L);
-    // segments of more than 8 tokens on tcgen05 (BF16, deduplicating, n > 8)
+    // segments of more than 8 tokens on tcgen05 (BF16, deduplicating, n > 8);
+    // their B operands come through TMA tensor maps: phase 1 all n hidden
+    // rows in one box, phase 2 boxes of 16, 32, 48 or 64 rows of aperm.  A
+    // driver that cannot encode them leaves the pass to the mma.sync CTAs
+    // alone (same outputs, up to the summation order).
     P.wide = (!fp8 && plan != nullptr && n > 8) ? 1 : 0;
     P.aperm = wsb + ws.aperm;
-    // phase 1: all n hidden rows in one box
-    if (P.wide && e == cudaSuccess) e = encode_act_map(&P.act_map[0], h, n, L.d, (n + 15) & ~15);
+    const int slots = n * (L.top_k + L.n_shared);
+    CUtensorMap down_maps[4];
+    if (P.wide) {
+      cudaError_t me = encode_act_map(&P.act_map[0], h, n, L.d, (n + 15) & ~15);
+      for (int j = 0; j < 4 && me == cudaSuccess; ++j)
+        me = encode_act_map(&down_maps[j], P.aperm, slots, L.inter, 16 * (j + 1));
+      if (me != cudaSuccess) P.wide = 0;
+    }
     P.early_shared = early_shared && plan != nullptr && !P.wide;
     P.ready = P.early_shared ? ready : nullptr;
     int32_t *ashift = reinterpret_cast<int32_t *>(wsb + ws.ashift);
@@ -193,7 +203,6 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.out = wsb + ws.inter;
     if (e == cudaSuccess) e = launch_expert_tc(fp8, 1, n_tiles, P, sms, stream);
     // E4M3: each slot's row of a into fp16 range, in place
-    const int slots = n * (L.top_k + L.n_shared);
     if (fp8 && e == cudaSuccess)
       e = launch_a16_scale(wsb + ws.inter, slots, L.inter, ashift, sms, stream);
     // phase 2: down over W2, K = I
@@ -205,9 +214,8 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.row_blocks = L.d / 64;
     P.act = wsb + ws.inter;
     P.out = wsb + ws.yslot;
-    // phase 2: boxes of 16, 32, 48 or 64 rows of aperm
-    for (int j = 0; j < 4 && P.wide && e == cudaSuccess; ++j)
-      e = encode_act_map(&P.act_map[j], P.aperm, slots, L.inter, 16 * (j + 1));
+    if (P.wide)
+      for (int j = 0; j < 4; ++j) P.act_map[j] = down_maps[j];
     if (e == cudaSuccess) e = launch_expert_tc(fp8, 2, n_tiles, P, sms, stream);
   }
   if (e == cudaSuccess)
