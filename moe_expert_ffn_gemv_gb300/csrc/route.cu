@@ -180,15 +180,21 @@ __global__ void __launch_bounds__(ROUTER_MAX_WARPS * 32, 2) route_plan_kernel(
                      w + int64_t(t) * k);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    group_counter[blockIdx.y] = 0u;
-    __threadfence();  // this group's ids and weights before its ticket
-    const unsigned int ticket = atomicAdd(counter, 1u);
-    s_last = ticket == gridDim.y - 1;
+  if (gridDim.y > 1) {
+    // more than one group: the last group to be ranked builds the plan (one
+    // group needs no second ticket: that CTA is the last)
+    if (threadIdx.x == 0) {
+      group_counter[blockIdx.y] = 0u;
+      __threadfence();  // this group's ids and weights before its ticket
+      const unsigned int ticket = atomicAdd(counter, 1u);
+      s_last = ticket == gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  } else if (threadIdx.x == 0) {
+    group_counter[0] = 0u;
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
   __shared__ PlanSmem S;
   if constexpr (BUDGET) {
     __shared__ BudgetSmem B;
