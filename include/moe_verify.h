@@ -285,12 +285,13 @@ moe_status moe_route_plan_budgeted(const moe_layer_desc *desc,
  * largest keeps all its bits (smaller ones, whose terms cannot reach the
  * output tolerance, lose bits or become 0).  Sums beyond fp32's range
  * become inf, as in an fp32 accumulation.
- * With BF16 weights and n > 8, an expert routed by more than 8 of the
+ * With BF16 weights and n >= 25, an expert routed by more than 8 of the
  * tokens (or the shared expert) is computed on the 5th-generation tensor
  * cores (tcgen05, accumulators in tensor memory) with all of its tokens at
  * once; its fp32 sums are then added in another order than on the mma.sync
- * path, so its outputs may differ from a pass that routes it fewer tokens
- * in the last bits.  A given call repeats bit for bit.
+ * path, so its outputs may differ in the last bits from a pass of fewer
+ * tokens or one that routes it fewer tokens.  A given call repeats bit for
+ * bit.
  * The kernels check the plan before they use its indices: U outside [0, N],
  * a uniq entry outside [0, N), offs decreasing, negative or past n*k, or a
  * perm entry outside [0, n*k) makes moe_last_error() report

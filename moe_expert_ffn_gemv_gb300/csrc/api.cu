@@ -19,6 +19,12 @@ constexpr int MAX_EXPERTS = 256;
 constexpr int MAX_TOPK = 32;
 constexpr int MAX_TOKENS = 64;
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000ull * 1000 * 1000;
+// Passes of fewer tokens run the mma.sync instance alone, whose segments of
+// 9-24 tokens take 2-3 passes over their weights: against it, the instance
+// with tcgen05 CTAs measured 3-8% slower at n = 9-16 (dedup calls and passes,
+// Qwen3- and OLMoE-shaped; 4-5% on 48-layer stacks), between -4% and +8% at
+// n = 17-24 depending on the tree, and never slower from n = 32 (to 25% faster).
+constexpr int WIDE_MIN_TOKENS = 25;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -169,12 +175,12 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
     P.T = T;
     P.err = err;
     P.timeout_ns = timeout_ns(L);
-    // segments of more than 8 tokens on tcgen05 (BF16, deduplicating, n > 8);
-    // their B operands come through TMA tensor maps: phase 1 all n hidden
-    // rows in one box, phase 2 boxes of 16, 32, 48 or 64 rows of aperm.  A
-    // driver that cannot encode them leaves the pass to the mma.sync CTAs
-    // alone (same outputs, up to the summation order).
-    P.wide = (!fp8 && plan != nullptr && n > 8) ? 1 : 0;
+    // Segments of more than 8 tokens on tcgen05 CTAs (BF16, deduplicating,
+    // n >= WIDE_MIN_TOKENS).  Their B operands come through TMA tensor maps:
+    // phase 1 all n hidden rows in one box, phase 2 boxes of 16, 32, 48 or
+    // 64 rows of aperm.  A driver that cannot encode them leaves the pass to
+    // the mma.sync CTAs alone (same outputs, up to the summation order).
+    P.wide = (!fp8 && plan != nullptr && n >= WIDE_MIN_TOKENS) ? 1 : 0;
     P.aperm = wsb + ws.aperm;
     const int slots = n * (L.top_k + L.n_shared);
     CUtensorMap down_maps[4];

@@ -39,13 +39,13 @@ def _pass(mv, layer, h, n, timeout_us):
     return y, vl.last_error()
 
 
-# A BF16 layer with a shared expert at 12 tokens: the shared expert's segment
+# A BF16 layer with a shared expert at 26 tokens: the shared expert's segment
 # (and any routed one of more than 8 tokens) runs on the tcgen05 CTAs.
 WIDE = synth.LayerConfig("bf16-wide-fault", 512, 12, 3, 192, synth.BF16, synth.BF16,
                          synth.GATE_SOFTMAX_RENORM, n_shared=1, hidden="tree_add", sigma=0.3)
 
 
-@pytest.mark.parametrize("cfg,n", [(SMALL, 8), (WIDE, 12)], ids=["fp8-n8", "bf16-tcgen05-n12"])
+@pytest.mark.parametrize("cfg,n", [(SMALL, 8), (WIDE, 26)], ids=["fp8-n8", "bf16-tcgen05-n26"])
 def test_tiny_wait_limit_ends_cleanly_then_normal_call_is_right(mv, cfg, n):
     layer = synth.make_layer(cfg, seed=4).to("cuda")
     h = synth.make_hidden(cfg, n, seed=5)
@@ -108,8 +108,8 @@ MALFORMED = ["uniq_out_of_range", "perm_out_of_range", "u_too_large", "offs_decr
 
 
 @pytest.mark.parametrize("cfg,n", [(SMALL, 6), (synth.shrink(synth.OLMOE, 512, 128), 6),
-                                   (synth.TINY, 6), (WIDE, 12)],
-                         ids=["fp8", "bf16", "f32", "bf16-tcgen05-n12"])
+                                   (synth.TINY, 6), (WIDE, 26)],
+                         ids=["fp8", "bf16", "f32", "bf16-tcgen05-n26"])
 @pytest.mark.parametrize("kind", MALFORMED)
 def test_a_malformed_caller_plan_is_reported_not_followed(mv, cfg, n, kind):
     # moe_verify_dedup takes any plan from its caller: the expert kernels

@@ -1,13 +1,15 @@
 """The tcgen05 CTAs of the BF16 deduplicating engine against the oracle.
 
-A segment of more than 8 tokens of a BF16 pass runs on tensor-memory CTAs
-(the first W of the grid) while the rest run the mma.sync path.  These cases
-aim at that split: the boundary (m = 8 stays narrow, m = 9 goes wide), a
-shared expert as a wide segment (its rows of the activation buffer sit behind
-the routed slots), a down projection with an odd number of 64-row blocks (the
-last row pair holds one tile), plans that mix wide and narrow segments, and
-the largest segment (64 tokens).  The oracle gets the GPU's routing, as in
-the other expert tests.
+A BF16 pass of 25 tokens or more runs its segments of more than 8 tokens on
+tensor-memory CTAs (the first W of the grid) while the rest run the mma.sync
+path; smaller passes run the mma.sync path alone.  These cases aim at that
+split: the segment-size boundary inside such a pass (8 tokens stay on the
+mma.sync CTAs, 9 go to the tcgen05 ones), the pass-size boundary (24 and 25
+tokens), a shared expert as a wide segment (its rows of the activation
+buffer sit behind the routed slots), a down projection with an odd number
+of 64-row blocks (the last row pair holds one tile), plans that mix wide and
+narrow segments, and the largest segment (64 tokens).  The oracle gets the
+GPU's routing (or the given one), as in the other expert tests.
 """
 import numpy as np
 import pytest
@@ -44,40 +46,76 @@ def get_layer(cfg):
     return _LAYERS[cfg]
 
 
-def run(mv, cfg, n, kind=None, sigma=None):
-    dev_layer, _, L = get_layer(cfg)
-    h = synth.make_hidden(cfg, n, seed=5, kind=kind, sigma=sigma)
-    ids, w, _, y_ref = oracle.verify(L, np_bytes(h), threads=THREADS)
+def run_routed(mv, cfg, h, ids, w, y_ref):
+    dev_layer, _, _ = get_layer(cfg)
+    n = h.shape[0]
     vl = mv.VerifyLayer(dev_layer, 64)
     vl.ids[:n * cfg.top_k].copy_(torch.from_numpy(ids.reshape(-1)).to(torch.int32))
-    vl.w[:n * cfg.top_k].copy_(torch.from_numpy(w.reshape(-1)).to(torch.float32))
+    vl.w[:n * cfg.top_k].copy_(torch.from_numpy(np.asarray(w).reshape(-1)).to(torch.float32))
     vl.union_plan(n)
     y = vl.dedup(h.cuda(), n)
     assert vl.last_error() == 0
     y = y.float().cpu().numpy().astype(np.float64)
     err = rel_err(y, y_ref)
     assert err <= TOL[cfg.wtype], f"{cfg.name} n={n}: rel err {err:.3g}"
-    counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
-    return y, counts
+    return y
 
 
-@pytest.mark.parametrize("n", [8, 9, 16, 33, 64])
-def test_identical_tokens_boundary(mv, n):
+def run(mv, cfg, n, kind=None, sigma=None):
+    _, _, L = get_layer(cfg)
+    h = synth.make_hidden(cfg, n, seed=5, kind=kind, sigma=sigma)
+    ids, w, _, y_ref = oracle.verify(L, np_bytes(h), threads=THREADS)
+    y = run_routed(mv, cfg, h, ids, w, y_ref)
+    return y, np.bincount(ids.ravel(), minlength=cfg.n_experts)
+
+
+def given_routing(n, k, n_experts, counts):
+    """ids [n][k]: expert e on counts[e] tokens (sum = n*k), k distinct
+    experts a token; each expert goes to the tokens with the fewest experts
+    so far (lowest index first)."""
+    assert sum(counts) == n * k and len(counts) == n_experts
+    rows = [[] for _ in range(n)]
+    for e in sorted(range(n_experts), key=lambda e: -counts[e]):
+        order = sorted(range(n), key=lambda t: (len(rows[t]), t))
+        picked = [t for t in order if len(rows[t]) < k][:counts[e]]
+        assert len(picked) == counts[e]
+        for t in picked:
+            rows[t].append(e)
+    assert all(len(r) == k for r in rows)
+    return np.asarray(rows, dtype=np.int32)
+
+
+def test_segment_size_boundary_inside_a_tcgen05_pass(mv):
+    # 32 tokens, given routing: segments of 1, 2, 8 and 9, 16 and 17, and 24
+    # tokens in one pass, so that 8 stays on the mma.sync CTAs and 9 goes to
+    # the tcgen05 ones
+    cfg, n = PLAIN, 32
+    counts = [9, 8, 17, 16, 24, 1, 2, 12, 12, 8, 6, 5, 4, 2, 1, 1]
+    ids = given_routing(n, cfg.top_k, cfg.n_experts, counts)
+    assert np.array_equal(np.bincount(ids.ravel(), minlength=cfg.n_experts), counts)
+    _, _, L = get_layer(cfg)
+    h = synth.make_hidden(cfg, n, seed=7)
+    w, _, y_ref = oracle.verify_routed(L, np_bytes(h), ids, threads=THREADS)
+    run_routed(mv, cfg, h, ids, w, y_ref)
+
+
+@pytest.mark.parametrize("n", [24, 25, 33, 64])
+def test_identical_tokens(mv, n):
     # one segment of n tokens per chosen expert (and the shared expert's):
-    # n = 8 runs on the mma.sync CTAs, n >= 9 on the tensor-memory CTAs
+    # n = 24 runs on the mma.sync CTAs alone, n >= 25 on the tcgen05 ones
     y, counts = run(mv, SHARED, n, kind="identical")
     assert sorted(counts[counts > 0].tolist()) == [n] * SHARED.top_k
     assert np.array_equal(y[0], y[n - 1])
 
 
-@pytest.mark.parametrize("n", [12, 24, 40, 64])
+@pytest.mark.parametrize("n", [25, 40, 64])
 def test_shared_expert_tree(mv, n):
     # the shared expert's segment (n tokens) is always wide here; the routed
     # segments of a correlated tree are a mix of both kinds
     run(mv, SHARED, n)
 
 
-@pytest.mark.parametrize("n,sigma", [(20, 0.3), (48, 0.3), (64, 0.05), (64, 1.0)])
+@pytest.mark.parametrize("n,sigma", [(28, 0.3), (48, 0.3), (64, 0.05), (64, 1.0)])
 def test_mixed_segments(mv, n, sigma):
     _, counts = run(mv, PLAIN, n, sigma=sigma)
     if sigma <= 0.3:
