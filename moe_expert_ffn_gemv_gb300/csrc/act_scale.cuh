@@ -85,6 +85,69 @@ __device__ __forceinline__ void act_scale_block(const __nv_bfloat16 *__restrict_
   }
 }
 
+// Token t's row of h [n][d] (bf16, d % 8 == 0, d <= 8 * ACT_ROW_THREADS *
+// ACT_ROW_WORDS), by the ACT_ROW_THREADS threads of the block: the row's
+// 16-byte words stay in registers between the maximum and the rewrite, so
+// the row is read once.  Same shift and same fp16 values as act_scale_block.
+constexpr int ACT_ROW_THREADS = 256;
+constexpr int ACT_ROW_WORDS = 4;  // 16-byte words a thread keeps: rows of up to 8192
+
+__device__ __forceinline__ void act_scale_row(const __nv_bfloat16 *__restrict__ h, int d, int t,
+                                              __half *__restrict__ h16, int32_t *hshift) {
+  __shared__ float s_part[ACT_ROW_THREADS / 32];
+  __shared__ int s_shift;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16 *row = h + int64_t(t) * d;
+  uint4 v[ACT_ROW_WORDS];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < ACT_ROW_WORDS; ++i) {
+    const int c = (i * ACT_ROW_THREADS + int(threadIdx.x)) * 8;
+    if (c < d) v[i] = __ldg(reinterpret_cast<const uint4 *>(row + c));
+  }
+#pragma unroll
+  for (int i = 0; i < ACT_ROW_WORDS; ++i) {
+    const int c = (i * ACT_ROW_THREADS + int(threadIdx.x)) * 8;
+    if (c < d) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        // fmaxf drops a NaN operand, so a NaN leaves the maximum alone
+        m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) s_part[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float x = 0.f;
+    for (int w = 0; w < ACT_ROW_THREADS / 32; ++w) x = fmaxf(x, s_part[w]);
+    const int sh = fp16_range_shift(__float_as_uint(x));
+    s_shift = sh;
+    hshift[t] = sh;
+  }
+  __syncthreads();
+  const float mul = pow2f(s_shift);
+#pragma unroll
+  for (int i = 0; i < ACT_ROW_WORDS; ++i) {
+    const int c = (i * ACT_ROW_THREADS + int(threadIdx.x)) * 8;
+    if (c < d) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 p = __floats2half2_rn(__uint_as_float(w[j] << 16) * mul,
+                                            __uint_as_float(w[j] & 0xFFFF0000u) * mul);
+        o[j] = *reinterpret_cast<const uint32_t *>(&p);
+      }
+      *reinterpret_cast<uint4 *>(h16 + int64_t(t) * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // One warp: row `slot` of a [slots][I] (bf16 as the gate/up kernel wrote
 // it; I % 8 == 0), rewritten in place as fp16 times 2^ashift[slot].  Each
 // lane handles its own 16-byte words: rows of up to 2048 elements are held

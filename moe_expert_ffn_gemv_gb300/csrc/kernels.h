@@ -106,7 +106,7 @@ struct ActScaleOut {
   unsigned int *acts;  // launch_route_plan: blocks written so far (null: none)
 };
 
-// The E4M3 engines' fp16 rows of h [n][d] (bf16), one CTA per 8 tokens,
+// The E4M3 engines' fp16 rows of h [n][d] (bf16, d <= 8192), one CTA per token,
 // launched as a programmatic dependent of the kernel ahead (it waits for
 // that kernel before reading h).  (act_scale.cu)
 cudaError_t launch_act_scale(const void *h, int n, int d, const ActScaleOut &S,
