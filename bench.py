@@ -212,7 +212,7 @@ def traffic_from_profile():
             for line in f:
                 if line.startswith("traffic_json:"):
                     j = json.loads(line.split(":", 1)[1])
-                    if j.get("dedup_kernels_sha256") == csrc_hash(DEDUP_KERNEL_SOURCES):
+                    if j.get("dedup_kernels_code_sha256") == code_hash(DEDUP_KERNEL_SOURCES):
                         return j.get("dram_bytes_per_dedup_call")
     except Exception:
         pass
@@ -233,6 +233,44 @@ def csrc_hash(names=None) -> str:
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments, each run of whitespace made
+    one space: what the compiler sees, give or take the preprocessor.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def code_hash(names) -> str:
+    """Hash of the named kernel sources with their comments left out, so
+    that a recorded measurement stays tied to the code, not to its prose."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "moe_expert_ffn_gemv_gb300", "csrc")
+    for name in sorted(names):
+        with open(os.path.join(d, name), encoding="utf-8") as f:
+            h.update(name.encode())
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -165,8 +165,9 @@ moe_status run_experts(const moe_layer_desc &L, const moe_expert_weights &W, con
       if (!early_shared) e = launch_act_scale(h, n, L.d, S, stream);
     }
     // One 8-token mma.sync tile per pass over a work item.  A BF16 segment of
-    // more tokens runs on tcgen05 CTAs, all its tokens in one pass (P.wide);
-    // an E4M3 one (the shared expert at n > 8) takes one pass per 8 tokens.
+    // more tokens in a pass of WIDE_MIN_TOKENS or more runs on tcgen05 CTAs,
+    // all its tokens in one pass (P.wide); otherwise (and for E4M3, e.g. the
+    // shared expert at n > 8) a segment takes one pass per 8 tokens.
     // Wider mma.sync tiles (2 or 4 per pass) fit in registers, but their
     // activation rows leave the ring 3 or 4 stages, and they measured slower
     // than the extra passes.

@@ -257,10 +257,11 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
 //
 // A segment of more than WIDE_M tokens (a popular routed expert in a
 // correlated draft tree, identical tokens, a shared expert at n > 8) would
-// stream its weights through the mma.sync path once per 8 tokens.  With BF16
-// weights it runs instead on the 5th-generation tensor cores, on CTAs of its
-// own (the first W of the grid), so that each weight row crosses the SM once
-// per pass:
+// stream its weights through the mma.sync path once per 8 tokens.  In the
+// WIDE instance (which the host launches for BF16 deduplicating passes of
+// 25 tokens or more) it runs instead on the 5th-generation tensor cores, on
+// CTAs of its own (the first W of the grid), so that each weight row crosses
+// the SM once per pass:
 //   - a work item is (segment, row pair): 128 weight rows, the packed tiles
 //     of row blocks 2p and 2p + 1, against all m <= 64 tokens of the segment;
 //   - a stage is one 128-byte column of K: the two tiles' 8 KB columns (one
@@ -737,9 +738,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const __grid_cons
   }
   LocalTables T{s_uniq, s_offs, s_tab, &s_U, P.T.n, P.T.k, P.T.n_experts, P.T.n_shared,
                 P.T.dedup, (!FP8 && WIDE) ? WIDE_M : 0x7fffffff};
-  // BF16 deduplicating passes of more than WIDE_M tokens (never the early-start
-  // mode): the first W CTAs take the wide segments on tcgen05; every CTA
-  // computes the same W from the plan.
+  // The WIDE instance (BF16 deduplicating passes the host picks, never the
+  // early-start mode): the first W CTAs take the segments of more than
+  // WIDE_M tokens on tcgen05; every CTA computes the same W from the plan.
   int W = 0;
   if constexpr (!FP8 && WIDE) {
     {

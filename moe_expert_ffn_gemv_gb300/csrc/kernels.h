@@ -58,7 +58,7 @@ struct TcParams {
   const int32_t *hshift;
   const int32_t *ashift;
   const uint32_t *acts;
-  // BF16 deduplicating pass of more than 8 tokens, not in the early-start
+  // BF16 deduplicating pass of 25 tokens or more, not in the early-start
   // mode: segments of more than 8 tokens run on tcgen05 CTAs (expert_tc.cu).
   // Their activations come in 2-D TMA boxes of 64 elements x 16 (j + 1) rows
   // through act_map[j] (128-byte swizzle): phase 1 the hidden states [n][d]
