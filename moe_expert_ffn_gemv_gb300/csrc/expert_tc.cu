@@ -667,14 +667,9 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const __grid_cons
   const bool acts_flag = FP8 && PHASE == 1 && lazy && P.acts != nullptr;
   auto await_acts = [&]() -> bool {
     const uint32_t need = uint32_t((P.T.n + 7) / 8);
-    bool seen = true;
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(P.acts) < need)
-      if (globaltimer_ns() - t0 > P.timeout_ns) {
-        seen = false;
-        break;
-      }
-    return __all_sync(0xffffffffu, seen);
+    const bool seen = await_flag(P.acts, need, P.timeout_ns);
+    if (seen) (void)ld_acquire_gpu(P.acts);  // this lane's own acquire (the count only grows)
+    return seen;
   };
   // the plan (or, per-slot, the ids) into shared memory, threads first,
   // first + step, ... (the early-start mode has its own loader, below)
@@ -975,16 +970,12 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const __grid_cons
     int since_plan = 0;  // stages issued since the plan arrived
     auto load_plan = [&]() -> bool {
       if (plan_ready) return true;
-      // every lane acquires the flag itself, so that its own plan reads
+      // lane 0 waits for the flag; then every lane acquires it itself (it
+      // stays raised until the pass's combine), so that its own plan reads
       // below are ordered after the plan kernel's writes
-      bool seen = true;
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_gpu(P.ready) == 0u)
-        if (globaltimer_ns() - t0 > P.timeout_ns) {
-          seen = false;
-          break;
-        }
-      if (!__all_sync(0xffffffffu, seen)) {
+      const bool seen = await_flag(P.ready, 1u, P.timeout_ns);
+      if (seen) (void)ld_acquire_gpu(P.ready);
+      if (!seen) {
         if (lane == 0) record_error(P.err, MOE_ERR_TIMEOUT);
         s_abort = 1;
         return false;

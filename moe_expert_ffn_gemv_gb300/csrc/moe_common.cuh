@@ -79,6 +79,26 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Called by a whole warp: lane 0 polls the device word *p (acquire, with a
+// short sleep between reads, so that many waiting warps do not crowd the
+// L2 slice that holds it) until it reaches `target` or `limit_ns` passes.
+// Returns, in every lane, whether it was reached.
+__device__ __forceinline__ bool await_flag(const uint32_t *p, uint32_t target,
+                                           uint64_t limit_ns) {
+  int seen = 1;
+  if ((threadIdx.x & 31) == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(p) < target) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        seen = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  return __shfl_sync(0xffffffffu, seen, 0) != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
