@@ -288,9 +288,11 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
 //     costs ~0.1-0.3 us under that traffic; one 4-byte store a column and
 //     lane held the first items up for 4-19 us).
 // W is the split of the grid with the shortest modelled makespan, a wide
-// item costing W_ITEM_COST hundredths of a narrow one: measured, a tensor-
-// memory CTA moves its (twice as large) items ~1.5x slower per byte than a
-// narrow CTA, with fewer weight bytes in flight (the B box shares the ring).
+// item costing W_ITEM_COST hundredths of a narrow one.  While both kinds
+// stream, HBM is saturated and a tensor-memory CTA completes a 16 KB stage
+// every ~0.42 us against ~0.7 us for a narrow CTA's 32 KB (its share of the
+// memory system: a 5-slot ring measured the same); with the start offsets,
+// the wide epilogue's tail and whole items per CTA, 3 measured best.
 // Every wait is bounded; after a time-out the warps keep walking their items
 // without waiting, so that all of them reach the final barrier, and the
 // tensor memory is freed only after every issued MMA has completed.
