@@ -3,10 +3,13 @@
 first expert kernel starts on the shared expert while routing still runs;
 the outputs must not change, and work enqueued before the call (a write of
 the hidden states) must be seen."""
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from moe_expert_ffn_gemv_gb300 import synth
+from tests.helpers import THREADS, TOL, np_bytes, oracle_layer, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -17,9 +20,13 @@ def mv():
     return binding
 
 
+# d = 8192: the widest E4M3 rows, every thread of the row-scaling CTAs on
+# its last 16-byte word (the pass scales rows in its plan kernel, the dedup
+# call in a kernel of its own: both must give the same rows and shifts)
 CASES = [synth.TINY, synth.shrink(synth.OLMOE, 512, 128),
          synth.shrink(synth.DSV3, 1024, 256, 64, "dsv3-pass"),
-         synth.shrink(synth.DSV3, 7168, 256, 16, "dsv3-wide")]
+         synth.shrink(synth.DSV3, 7168, 256, 16, "dsv3-wide"),
+         synth.shrink(synth.DSV3, 8192, 256, 16, "dsv3-d8192")]
 
 
 def separate(vl, h, n, budget):
@@ -75,3 +82,22 @@ def test_verify_pass_empty(mv):
     vl.verify_pass(torch.empty(0, 512, dtype=torch.bfloat16, device="cuda"), 0)
     torch.cuda.synchronize()
     assert int(vl.plan.n_uniq[0]) == 0
+
+
+@pytest.mark.parametrize("d,n", [(8192, 8), (8064, 13)])
+def test_widest_e4m3_rows_match_the_oracle(mv, d, n):
+    # the largest hidden size E4M3 layers take (8192), and one whose rows
+    # end inside the row-scaling threads' last word, over two token groups
+    cfg = synth.shrink(synth.DSV3, d, 256, 8, f"dsv3-d{d}")
+    layer = synth.make_layer(cfg, seed=26)
+    h = synth.make_hidden(cfg, n, seed=27)
+    ids, w, _, y_ref = oracle.verify(oracle_layer(layer), np_bytes(h), threads=THREADS)
+    vl = mv.VerifyLayer(layer.to("cuda"), 16)
+    hd = h.cuda()
+    vl.ids[:n * cfg.top_k].copy_(torch.from_numpy(ids.reshape(-1)).to(torch.int32))
+    vl.w[:n * cfg.top_k].copy_(torch.from_numpy(np.asarray(w).reshape(-1)).to(torch.float32))
+    vl.union_plan(n)
+    y = vl.dedup(hd, n).float().cpu().numpy().astype(np.float64)
+    assert vl.last_error() == 0
+    err = rel_err(y, y_ref)
+    assert err <= TOL[synth.E4M3], f"d={d} n={n}: rel err {err:.3g}"
