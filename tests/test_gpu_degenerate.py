@@ -75,3 +75,37 @@ def test_degenerate_routing(mv, cfg, n):
     assert int(vl.plan.n_uniq[0]) == N
     err = rel_err(y.astype(np.float64), y_ref)
     assert err <= TOL[cfg.wtype], f"{cfg.name} n={n} pass: rel err {err:.3g}"
+
+
+LARGEST = [
+    synth.LayerConfig("fp8-k32-shared", 256, 64, 32, 128, synth.BF16, synth.E4M3,
+                      synth.GATE_SIGMOID_RENORM, n_shared=1, hidden="tree_ar", rho=0.6),
+    synth.LayerConfig("bf16-k32-shared", 256, 64, 32, 128, synth.BF16, synth.BF16,
+                      synth.GATE_SOFTMAX_RENORM, n_shared=1, hidden="tree_add", sigma=0.3),
+]
+
+
+@pytest.mark.parametrize("cfg", LARGEST, ids=lambda c: c.name)
+def test_largest_plan_the_abi_takes(mv, cfg):
+    # n = 64 tokens, k = 32 (both at their limits) and a shared expert: 2048
+    # routed slots and 64 shared ones, the most every table of the expert
+    # kernels holds; with BF16 weights most segments (about 32 tokens each)
+    # run on the tcgen05 CTAs, whose activation maps then span 2112 rows
+    n = 64
+    layer = synth.make_layer(cfg, seed=4, device="cpu")
+    h = synth.make_hidden(cfg, n, seed=6)
+    ids, w, _, y_ref = oracle.verify(oracle_layer(layer), np_bytes(h), threads=THREADS)
+    dev = layer.to("cuda")
+    vl = mv.VerifyLayer(dev, 64)
+    hd = h.cuda()
+    k = cfg.top_k
+    vl.ids[:n * k].copy_(torch.from_numpy(ids.reshape(-1)).to(torch.int32))
+    vl.w[:n * k].copy_(torch.from_numpy(w.reshape(-1)).to(torch.float32))
+    vl.union_plan(n)
+    counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
+    assert int(vl.plan.n_uniq[0]) == int((counts > 0).sum())
+    for engine in ("dedup", "perslot"):
+        y = (vl.dedup(hd, n) if engine == "dedup" else vl.perslot(hd, n)).float().cpu().numpy()
+        assert vl.last_error() == mv.MOE_OK
+        err = rel_err(y.astype(np.float64), y_ref)
+        assert err <= TOL[cfg.wtype], f"{cfg.name} {engine}: rel err {err:.3g}"
