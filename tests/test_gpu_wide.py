@@ -99,6 +99,20 @@ def test_segment_size_boundary_inside_a_tcgen05_pass(mv):
     run_routed(mv, cfg, h, ids, w, y_ref)
 
 
+def test_down_projection_box_boundaries(mv):
+    # 64 tokens, given routing: segments of 64, 49, 48, 33, 32 and 17 tokens,
+    # each at or just past the edge of a 16/32/48/64-row activation box of
+    # the down projection, beside narrow segments of 8 and 5
+    cfg, n = PLAIN, 64
+    counts = [64, 49, 48, 33, 32, 17, 8, 5] + [0] * 8
+    ids = given_routing(n, cfg.top_k, cfg.n_experts, counts)
+    assert np.array_equal(np.bincount(ids.ravel(), minlength=cfg.n_experts), counts)
+    _, _, L = get_layer(cfg)
+    h = synth.make_hidden(cfg, n, seed=8)
+    w, _, y_ref = oracle.verify_routed(L, np_bytes(h), ids, threads=THREADS)
+    run_routed(mv, cfg, h, ids, w, y_ref)
+
+
 @pytest.mark.parametrize("n", [24, 25, 33, 64])
 def test_identical_tokens(mv, n):
     # one segment of n tokens per chosen expert (and the shared expert's):
