@@ -147,3 +147,22 @@ def test_repeat_is_bitwise_stable(mv):
     y2 = vl.dedup(h, 48).clone()
     assert vl.last_error() == 0
     assert torch.equal(y1, y2)
+
+
+def test_pass_with_tcgen05_ctas_replays_from_a_cuda_graph(mv):
+    # the tensor maps of the activation boxes are kernel parameters, recorded
+    # with the graph: replays on new hidden states (written into the same
+    # buffer) must match the eager pass bit for bit
+    dev_layer, _, _ = get_layer(PLAIN)
+    n = 48
+    vl = mv.VerifyLayer(dev_layer, 64)
+    h = torch.empty(n, PLAIN.d, dtype=torch.bfloat16, device="cuda")
+    h.copy_(synth.make_hidden(PLAIN, n, seed=11))
+    g = vl.capture_pass(h, n)
+    for seed in (12, 13):
+        h.copy_(synth.make_hidden(PLAIN, n, seed=seed))
+        g.replay()
+        y_graph = vl.y[:n].clone()
+        y_eager = vl.verify_pass(h, n).clone()
+        assert vl.last_error() == 0
+        assert torch.equal(y_graph, y_eager)
