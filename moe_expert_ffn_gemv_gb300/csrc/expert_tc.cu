@@ -292,7 +292,7 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
 // stream, HBM is saturated and a tensor-memory CTA completes a 16 KB stage
 // every ~0.42 us against ~0.7 us for a narrow CTA's 32 KB (its share of the
 // memory system: a 5-slot ring measured the same); with the start offsets,
-// the wide epilogue's tail and whole items per CTA, 3 measured best.
+// the wide epilogue's tail and whole items per CTA, 3 measured best overall.
 // Every wait is bounded; after a time-out the warps keep walking their items
 // without waiting, so that all of them reach the final barrier, and the
 // tensor memory is freed only after every issued MMA has completed.
