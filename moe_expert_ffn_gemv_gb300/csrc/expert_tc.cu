@@ -288,7 +288,8 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const LocalTables &T, int
 //     costs ~0.1-0.3 us under that traffic; one 4-byte store a column and
 //     lane held the first items up for 4-19 us).
 // W is the split of the grid with the shortest modelled makespan, a wide
-// item costing W_ITEM_COST hundredths of a narrow one.  While both kinds
+// item costing W_ITEM_COST_P1 (gate/up) or W_ITEM_COST_P2 (down) hundredths
+// of a narrow one.  While both kinds
 // stream, HBM is saturated and a tensor-memory CTA completes a 16 KB stage
 // every ~0.42 us against ~0.7 us for a narrow CTA's 32 KB (its share of the
 // memory system: a 5-slot ring measured the same); with the start offsets,
@@ -304,9 +305,14 @@ constexpr int W_A_BYTES = 16384;  // 128 rows x 128 bytes of K
 // bytes; as many slots as fit (at most W_MAX_STAGES) keep 110-180 KB of
 // weights in flight, as the mma.sync CTAs do (160 KB).
 constexpr int W_MAX_STAGES = 12;
-// the modelled cost of a wide item, in hundredths of a narrow item's (the
-// best of 200-500 on Qwen3/OLMoE-shaped trees of 12-64 tokens)
-constexpr int W_ITEM_COST = 300;
+// the modelled cost of a wide item, in hundredths of a narrow item's, for
+// the gate/up and the down kernel: the best of 230-360 (gate/up) and
+// 240-500 (down) on Qwen3- and OLMoE-shaped trees of 25-64 tokens.  A down
+// cost of 360 against 300 took OLMoE rho = 0.9 n = 32 from 119.5 to
+// 112.3 us and Qwen3 sigma = 1.0 n = 64 from 166.6 to 159.4 us (dedup
+// calls), and left the others level.
+constexpr int W_ITEM_COST_P1 = 300;
+constexpr int W_ITEM_COST_P2 = 360;
 constexpr int W_AVAIL =
     int(n_stages<false, 1>() * size_t(slot_bytes<false, 1>()) + n_red_bufs<false, 1>() * red_bytes<1>()) -
     1024;
@@ -761,7 +767,7 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const __grid_cons
           wi += __shfl_xor_sync(0xffffffffu, wi, o);
         }
         // W: the split of the grid with the shortest modelled makespan, a
-        // wide item (two row blocks) costing W_ITEM_COST hundredths of a
+        // wide item (two row blocks) costing W_ITEM_COST_P1/_P2 hundredths of a
         // narrow one (one row block, one token group); each lane tries every
         // 32nd W, the warp takes the best (ties to the smaller W)
         const int G = gridDim.x;
@@ -770,7 +776,8 @@ __global__ void __launch_bounds__(THREADS, 1) expert_tc_kernel(const __grid_cons
           best_w = min(G, wi);
         } else if (wi > 0) {
           for (int w = 1 + lane; w < G && w <= wi; w += 32) {
-            const int t = max(W_ITEM_COST * ((wi + w - 1) / w), 100 * ((nb + (G - w) - 1) / (G - w)));
+            const int t = max((PHASE == 1 ? W_ITEM_COST_P1 : W_ITEM_COST_P2) * ((wi + w - 1) / w),
+                              100 * ((nb + (G - w) - 1) / (G - w)));
             if (t < best_t) { best_t = t; best_w = w; }
           }
         }
